@@ -1,0 +1,190 @@
+"""fp64 CPU oracle for MLA tree-verify attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA path
+(``mla_speculative_decode_gb300``) and imports nothing from it; the product
+path never imports it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, one thread
+per group of output rows).  This module only compiles that file with gcc and
+marshals numpy arrays into it.  bf16 tensors cross as their raw 16-bit
+patterns (numpy ``uint16``); the C side widens them exactly.
+
+Functions and the passages they follow (page titles and sections):
+  tree_bits     -- The Checkpoint Report, "Mistakes and Incorrect Assumptions"
+                   (draft rows of the extend mask) and "Input Knowledge
+                   Required" (the DDTree draft tree).
+  verify_attn   -- The Milestone Commit, "Input Knowledge Required" (attention
+                   of the draft tokens against the full KV cache) and
+                   "Context" (MLA latent cache, page_size=1 slots).
+  lse_merge     -- The Commit That Locked In 6x Decode, "Input Knowledge
+                   Required" (NSPLIT partial-reduce); The Milestone Commit,
+                   "The Deeper Significance" (reduction kernel).
+  defrag        -- The Checkpoint Report, "Input Knowledge Required" (KV
+                   defragmentation keeps per-request KV contiguous).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+D_QK = 576   # latent 512 + rotary 64
+D_V = 512    # value = first 512 columns of the latent row
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library with gcc (no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.oracle_tree_bits.argtypes = [P, i32, P]
+    lib.oracle_tree_bits.restype = i32
+    lib.oracle_verify_attn.argtypes = [P, P, i64, i64, P, P, P, P, i32, i32, i32, i32, i32,
+                                       dbl, i64, i64, P, i64, P, P, i32]
+    lib.oracle_verify_attn.restype = i64
+    lib.oracle_lse_merge.argtypes = [i32, P, P, i32, P, P]
+    lib.oracle_lse_merge.restype = None
+    lib.oracle_defrag.argtypes = [P, i64, i64, P, P, P, i32, P]
+    lib.oracle_defrag.restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def tree_bits(parent) -> tuple[np.ndarray, int]:
+    """parent int32 [B, T] (or [T]) -> (ancestor-or-self bits uint64 same shape, #bad parents)."""
+    par = _c(parent, np.int32)
+    shape = par.shape
+    par2 = par.reshape(-1, shape[-1])
+    out = np.zeros(par2.shape, dtype=np.uint64)
+    lib = _load()
+    bad = 0
+    for b in range(par2.shape[0]):
+        row = np.ascontiguousarray(par2[b])
+        ob = np.zeros(shape[-1], dtype=np.uint64)
+        bad += lib.oracle_tree_bits(_ptr(row), int(shape[-1]), _ptr(ob))
+        out[b] = ob
+    return out.reshape(shape), bad
+
+
+def verify_attn(q_bits, kv_bits, slots, kv_indptr, prefix_len, bits, sm_scale: float,
+                k0: int = 0, k1: int = np.iinfo(np.int64).max,
+                rows: Optional[Sequence[int]] = None, threads: Optional[int] = None):
+    """Masked softmax attention of every (request, node, head) row.
+
+    q_bits   uint16 [B*T, H, 576]      bf16 bit patterns
+    kv_bits  uint16 [num_slots, stride] bf16 bit patterns (stride >= 576)
+    slots    int32  [sum_b N_b]         request b's keys: prefix slots then T tree slots
+    kv_indptr int   [B+1]               offsets of each request in ``slots``
+    prefix_len int  [B]
+    bits     uint64 [B, T]              ancestor-or-self sets
+    Returns (out float64 [rows, 512], lse float64 [rows], skipped_keys).
+    ``rows`` selects flat row indices ((b*T + i)*H + h); default all rows.
+    ``[k0, k1)`` restricts every request to that window of key indices.
+    """
+    q = _c(q_bits, np.uint16)
+    kv = _c(kv_bits, np.uint16)
+    assert q.ndim == 3 and q.shape[2] == D_QK, q.shape
+    assert kv.ndim == 2 and kv.shape[1] >= D_QK, kv.shape
+    bits_ = _c(bits, np.uint64)
+    B, T = bits_.shape
+    H = q.shape[1]
+    assert q.shape[0] == B * T
+    sl = _c(slots, np.int32)
+    ip = _c(kv_indptr, np.int64)
+    pl = _c(prefix_len, np.int32)
+    assert ip.shape == (B + 1,) and pl.shape == (B,)
+    if rows is None:
+        rows_arr = None
+        nrows = B * T * H
+    else:
+        rows_arr = _c(rows, np.int64)
+        nrows = rows_arr.shape[0]
+    out = np.zeros((nrows, D_V), dtype=np.float64)
+    lse = np.zeros((nrows,), dtype=np.float64)
+    lib = _load()
+    skipped = lib.oracle_verify_attn(
+        _ptr(q), _ptr(kv), kv.shape[0], kv.shape[1], _ptr(sl), _ptr(ip), _ptr(pl),
+        _ptr(bits_), B, T, H, D_QK, D_V, float(sm_scale), int(k0), int(k1),
+        _ptr(rows_arr) if rows_arr is not None else None, nrows, _ptr(out), _ptr(lse),
+        int(threads or default_threads()))
+    if skipped < 0:
+        raise ValueError("oracle_verify_attn: bad arguments")
+    return out, lse, int(skipped)
+
+
+def lse_merge(lse_parts, o_parts):
+    """lse_parts [S, rows], o_parts [S, rows, Dv] -> (out [rows, Dv], lse [rows])."""
+    lp = _c(lse_parts, np.float64)
+    op = _c(o_parts, np.float64)
+    S, nrows = lp.shape
+    Dv = op.shape[2]
+    out = np.zeros((nrows, Dv), dtype=np.float64)
+    lse = np.zeros((nrows,), dtype=np.float64)
+    lib = _load()
+    for r in range(nrows):
+        lr = np.ascontiguousarray(lp[:, r])
+        orr = np.ascontiguousarray(op[:, r, :])
+        o1 = np.zeros(Dv, dtype=np.float64)
+        l1 = np.zeros(1, dtype=np.float64)
+        lib.oracle_lse_merge(S, _ptr(lr), _ptr(orr), Dv, _ptr(o1), _ptr(l1))
+        out[r] = o1
+        lse[r] = l1[0]
+    return out, lse
+
+
+def defrag(pool_bits, src_slots, src_indptr, dst_base):
+    """Out-of-place compaction: returns (new pool uint16 copy, new slot table int32)."""
+    pool = np.array(pool_bits, dtype=np.uint16, copy=True, order="C")
+    src = _c(src_slots, np.int32)
+    ip = _c(src_indptr, np.int64)
+    db = _c(dst_base, np.int64)
+    B = db.shape[0]
+    slots_out = np.array(src, dtype=np.int32, copy=True)
+    lib = _load()
+    rc = lib.oracle_defrag(_ptr(pool), pool.shape[0], pool.shape[1], _ptr(src), _ptr(ip),
+                           _ptr(db), B, _ptr(slots_out))
+    if rc != 0:
+        raise ValueError("oracle_defrag: slot out of range")
+    return pool, slots_out
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,409 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each test would fail on a plausible mistake in the oracle: a dropped rotary
+term, a wrong scale, a mask off by one, a transposed operand, a wrong LSE
+base, a wrong merge weight.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import _brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _parse(path):
+    out = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = v.strip()
+    return out
+
+
+def _tiny(B=1, H=2, T=3, prefix=(5,), tree="random", seed=11, num_slots=64, stride=576, scale=None):
+    s = synth.Spec("pin", B=B, H=H, T=T, prefix=list(prefix), num_slots=num_slots, tree=tree,
+                   seed=seed, row_stride=stride)
+    w = synth.make(s)
+    if scale is not None:
+        w.spec.sm_scale = scale
+    return w
+
+
+def _run(oracle_mod, w, **kw):
+    bits, bad = oracle_mod.tree_bits(w.parents.numpy())
+    assert bad == 0
+    out, lse, skipped = oracle_mod.verify_attn(
+        synth.as_u16(w.q), synth.as_u16(w.kv_pool), w.slot_idx.numpy(), w.kv_indptr.numpy(),
+        w.prefix_len.numpy(), bits, w.spec.sm_scale, **kw)
+    return out, lse, skipped
+
+
+def _dense_mask(parent, P):
+    """Visibility [T, P+T] via transitive closure of the parent relation
+    (boolean matrix powers), independent of walking parent links."""
+    T = len(parent)
+    A = np.zeros((T, T), dtype=bool)
+    for i, p in enumerate(parent):
+        if p >= 0:
+            A[i, p] = True
+    reach = np.eye(T, dtype=bool)
+    step = np.eye(T, dtype=bool)
+    for _ in range(T):
+        step = (step.astype(np.int64) @ A.astype(np.int64)) > 0
+        reach |= step
+    m = np.zeros((T, P + T), dtype=bool)
+    m[:, :P] = True
+    m[:, P:] = reach
+    return m
+
+
+def _np_inputs(w):
+    q = w.q.to(torch.float64).numpy()                   # [B*T, H, 576]
+    kv = w.kv_pool.to(torch.float64).numpy()[:, :576]
+    return q, kv
+
+
+# ---------------------------------------------------------------- tree sets
+
+def test_tree_bits_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "tree_small.txt"))
+    parent = np.array([int(x) for x in g["parent"].split()], dtype=np.int32)
+    want = np.array([int(x) for x in g["bits"].split()], dtype=np.uint64)
+    bits, bad = oracle_mod.tree_bits(parent)
+    assert bad == 0
+    np.testing.assert_array_equal(bits, want)
+
+
+def test_tree_bits_vs_topdown_paths(oracle_mod):
+    gen = torch.Generator().manual_seed(3)
+    for T in (1, 2, 5, 17, 33, 64):
+        for tree in ("random", "chain", "flat"):
+            parent = synth.make_parents(T, tree, gen).tolist()
+            bits, bad = oracle_mod.tree_bits(np.array(parent, dtype=np.int32))
+            assert bad == 0
+            paths = _brute.tree_paths(parent)
+            for i in range(T):
+                assert int(bits[i]) == sum(1 << k for k in paths[i]), (T, tree, i)
+
+
+def test_tree_bits_bad_parent_counted(oracle_mod):
+    parent = np.array([-1, 0, 5, 1, -3], dtype=np.int32)   # node 2 forward, node 4 < -1
+    bits, bad = oracle_mod.tree_bits(parent)
+    assert bad == 2
+    assert int(bits[2]) == 1 << 2 and int(bits[4]) == 1 << 4
+    assert int(bits[3]) == (1 << 3) | (1 << 1) | 1
+
+
+def test_extend_mask_golden_through_attention(oracle_mod):
+    """q = 0 gives uniform weights over the visible keys; one-hot value rows then
+    read the visible set straight out of the attention output."""
+    g = _parse(os.path.join(GOLDEN, "extend_mask_small.txt"))
+    P = int(g["prefix"])
+    parent = np.array([int(x) for x in g["parent"].split()], dtype=np.int32)
+    T = len(parent)
+    rows = [np.array([int(x) for x in g[f"row{i}"].split()]) for i in range(T)]
+    N = P + T
+    kv = torch.zeros(N, 576, dtype=torch.bfloat16)
+    for j in range(N):
+        kv[j, j] = 1.0
+    q = torch.zeros(T, 1, 576, dtype=torch.bfloat16)
+    bits, _ = oracle_mod.tree_bits(parent[None])
+    out, lse, _ = oracle_mod.verify_attn(synth.as_u16(q), synth.as_u16(kv), np.arange(N, dtype=np.int32),
+                                         np.array([0, N]), np.array([P]), bits, 0.1)
+    for i in range(T):
+        vis = rows[i].astype(bool)
+        np.testing.assert_allclose(out[i, :N], vis / vis.sum(), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(out[i, N:], 0.0, atol=0)
+        assert abs(lse[i] - math.log(vis.sum())) < 1e-15
+
+
+# ------------------------------------------------------ brute force / library
+
+@pytest.mark.parametrize("seed,H,T,P,tree", [(1, 2, 3, 4, "random"), (2, 1, 4, 0, "random"),
+                                             (3, 3, 2, 6, "chain"), (4, 2, 5, 1, "flat")])
+def test_oracle_vs_pure_python_brute_force(oracle_mod, seed, H, T, P, tree):
+    w = _tiny(H=H, T=T, prefix=(P,), tree=tree, seed=seed, num_slots=32)
+    out, lse, _ = _run(oracle_mod, w)
+    qb = synth.as_u16(w.q).astype(int).tolist()
+    kb = synth.as_u16(w.kv_pool).astype(int).tolist()
+    bo, bl = _brute.brute_attention(qb, kb, w.slot_idx.tolist(), w.kv_indptr.tolist(),
+                                    w.prefix_len.tolist(), w.parents.tolist(), w.spec.sm_scale)
+    np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
+
+
+def test_oracle_vs_torch_sdpa_fp64(oracle_mod):
+    """Library routine: fp64 scaled_dot_product_attention with an explicit mask
+    built by transitive closure; lse from torch.logsumexp of the masked logits."""
+    w = _tiny(B=2, H=3, T=6, prefix=(9, 4), seed=5, num_slots=128)
+    out, lse, _ = _run(oracle_mod, w)
+    q, kv = _np_inputs(w)
+    B, T, H = 2, 6, 3
+    r = 0
+    for b in range(B):
+        P = int(w.prefix_len[b])
+        N = P + T
+        sl = w.slot_idx[int(w.kv_indptr[b]):int(w.kv_indptr[b]) + N].long()
+        K = torch.from_numpy(kv)[sl]                                  # [N, 576]
+        Q = torch.from_numpy(q[b * T:(b + 1) * T]).permute(1, 0, 2)   # [H, T, 576]
+        mask = torch.from_numpy(_dense_mask(w.parents[b].tolist(), P))
+        o = torch.nn.functional.scaled_dot_product_attention(
+            Q, K.expand(H, N, 576), K[:, :512].expand(H, N, 512), attn_mask=mask,
+            scale=w.spec.sm_scale)                                     # [H, T, 512]
+        logits = (Q @ K.T) * w.spec.sm_scale
+        l = torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1)  # [H, T]
+        o_rows = o.permute(1, 0, 2).reshape(T * H, 512).numpy()
+        l_rows = l.permute(1, 0).reshape(T * H).numpy()
+        np.testing.assert_allclose(out[r:r + T * H], o_rows, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[r:r + T * H], l_rows, rtol=0, atol=1e-12)
+        r += T * H
+
+
+def test_rotary_columns_enter_scores(oracle_mod):
+    """Changing only the 64 rotary columns of q changes the result; changing
+    columns beyond 576 of a wider pool row does not."""
+    w = _tiny(H=2, T=3, prefix=(4,), seed=21, stride=640)
+    out0, lse0, _ = _run(oracle_mod, w)
+    w.kv_pool[:, 576:] = 7.0
+    out1, lse1, _ = _run(oracle_mod, w)
+    np.testing.assert_array_equal(out0, out1)
+    w.q[:, :, 512:] *= -1.0
+    out2, lse2, _ = _run(oracle_mod, w)
+    assert np.abs(lse2 - lse0).max() > 1e-3
+
+
+# ------------------------------------------------------------- identities
+
+def test_chain_tree_equals_causal(oracle_mod):
+    """A chain-shaped tree is bottom-right aligned causal attention: node i sees
+    keys 0 .. P+i."""
+    from scipy.special import logsumexp, softmax
+    P, T, H = 7, 5, 2
+    w = _tiny(H=H, T=T, prefix=(P,), tree="chain", seed=8, num_slots=64)
+    out, lse, _ = _run(oracle_mod, w)
+    q, kv = _np_inputs(w)
+    K = kv[w.slot_idx.numpy()]
+    causal = np.tril(np.ones((T, P + T), dtype=bool), k=P)
+    for i in range(T):
+        for h in range(H):
+            s = w.spec.sm_scale * (K @ q[i, h])
+            s = np.where(causal[i], s, -np.inf)
+            np.testing.assert_allclose(out[i * H + h], softmax(s) @ K[:, :512], rtol=0, atol=1e-12)
+            assert abs(lse[i * H + h] - logsumexp(s)) < 1e-12
+
+
+def test_single_node_equals_decode(oracle_mod):
+    """T = 1: plain decode attention over all P + 1 keys."""
+    from scipy.special import logsumexp, softmax
+    P, H = 9, 3
+    w = _tiny(H=H, T=1, prefix=(P,), seed=9, num_slots=64)
+    out, lse, _ = _run(oracle_mod, w)
+    q, kv = _np_inputs(w)
+    K = kv[w.slot_idx.numpy()]
+    for h in range(H):
+        s = w.spec.sm_scale * (K @ q[0, h])
+        np.testing.assert_allclose(out[h], softmax(s) @ K[:, :512], rtol=0, atol=1e-12)
+        assert abs(lse[h] - logsumexp(s)) < 1e-12
+
+
+def test_slot_relocation_is_exact(oracle_mod):
+    """Moving rows to other pool slots and remapping the table gives identical bits."""
+    w = _tiny(B=2, H=2, T=4, prefix=(6, 3), seed=12, num_slots=64)
+    out0, lse0, _ = _run(oracle_mod, w)
+    perm = torch.randperm(64, generator=torch.Generator().manual_seed(1))
+    newpool = torch.empty_like(w.kv_pool)
+    newpool[perm] = w.kv_pool
+    w.kv_pool = newpool
+    w.slot_idx = perm[w.slot_idx.long()].to(torch.int32)
+    out1, lse1, _ = _run(oracle_mod, w)
+    np.testing.assert_array_equal(out0, out1)
+    np.testing.assert_array_equal(lse0, lse1)
+
+
+def test_prefix_order_invariance(oracle_mod):
+    w = _tiny(H=2, T=3, prefix=(11,), seed=13, num_slots=64)
+    out0, lse0, _ = _run(oracle_mod, w)
+    perm = torch.randperm(11, generator=torch.Generator().manual_seed(2))
+    w.slot_idx[:11] = w.slot_idx[:11][perm]
+    out1, lse1, _ = _run(oracle_mod, w)
+    np.testing.assert_allclose(out0, out1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse0, lse1, rtol=0, atol=1e-12)
+
+
+def test_tree_key_order_matters(oracle_mod):
+    """Swapping the slots of two tree nodes must change the result (the mask is
+    positional over the tree keys) -- guards against a mask that ignores k."""
+    w = _tiny(H=1, T=3, prefix=(2,), tree="chain", seed=14, num_slots=32)
+    out0, _, _ = _run(oracle_mod, w)
+    a, b = int(w.slot_idx[2]), int(w.slot_idx[4])
+    w.slot_idx[2], w.slot_idx[4] = b, a
+    out1, _, _ = _run(oracle_mod, w)
+    assert np.abs(out0 - out1).max() > 1e-6
+
+
+def test_head_permutation(oracle_mod):
+    w = _tiny(H=4, T=3, prefix=(5,), seed=15, num_slots=64)
+    out0, lse0, _ = _run(oracle_mod, w)
+    perm = torch.tensor([2, 0, 3, 1])
+    w.q = w.q[:, perm].contiguous()
+    out1, lse1, _ = _run(oracle_mod, w)
+    T, H = 3, 4
+    o0 = out0.reshape(T, H, 512)[:, perm.numpy()]
+    np.testing.assert_array_equal(o0.reshape(-1, 512), out1)
+    np.testing.assert_array_equal(lse0.reshape(T, H)[:, perm.numpy()].reshape(-1), lse1)
+
+
+# ----------------------------------------------------------- split algebra
+
+def test_lse_merge_of_splits_equals_unsplit(oracle_mod):
+    w = _tiny(B=1, H=2, T=5, prefix=(23,), seed=16, num_slots=64)
+    out, lse, _ = _run(oracle_mod, w)
+    N = 28
+    gen = np.random.default_rng(0)
+    for trial in range(4):
+        cuts = sorted(set([0, N] + list(gen.integers(0, N + 1, size=trial + 2))))
+        cuts = [0] + cuts if cuts[0] != 0 else cuts
+        # add an empty split and a split entirely past the end
+        windows = list(zip(cuts[:-1], cuts[1:])) + [(5, 5), (N, N + 10)]
+        lps, ops = [], []
+        for k0, k1 in windows:
+            o, l, _ = _run(oracle_mod, w, k0=k0, k1=k1)
+            lps.append(l)
+            ops.append(o)
+        mo, ml = oracle_mod.lse_merge(np.stack(lps), np.stack(ops))
+        np.testing.assert_allclose(mo, out, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(ml, lse, rtol=0, atol=1e-12)
+
+
+def test_lse_merge_closed_forms(oracle_mod):
+    o = np.array([[[1.0, -2.0]], [[3.0, 4.0]]])
+    lp = np.array([[0.5], [0.5]])
+    mo, ml = oracle_mod.lse_merge(lp, o)
+    assert abs(ml[0] - (0.5 + math.log(2.0))) < 1e-15
+    np.testing.assert_allclose(mo[0], [2.0, 1.0], atol=1e-15)
+    lp2 = np.array([[math.log(3.0)], [-np.inf]])
+    mo2, ml2 = oracle_mod.lse_merge(lp2, o)
+    assert abs(ml2[0] - math.log(3.0)) < 1e-15
+    np.testing.assert_allclose(mo2[0], o[0, 0], atol=0)
+    mo3, ml3 = oracle_mod.lse_merge(np.full((2, 1), -np.inf), o)
+    assert ml3[0] == -np.inf and np.all(mo3 == 0)
+
+
+# ------------------------------------------------------------ closed forms
+
+def test_zero_query_gives_mean_of_visible_values(oracle_mod):
+    P, T, H = 6, 4, 2
+    w = _tiny(H=H, T=T, prefix=(P,), seed=17, num_slots=64)
+    w.q.zero_()
+    out, lse, _ = _run(oracle_mod, w)
+    _, kv = _np_inputs(w)
+    K = kv[w.slot_idx.numpy()]
+    mask = _dense_mask(w.parents[0].tolist(), P)
+    for i in range(T):
+        vis = mask[i]
+        for h in range(H):
+            np.testing.assert_allclose(out[i * H + h], K[vis, :512].mean(0), rtol=0, atol=1e-13)
+            assert abs(lse[i * H + h] - math.log(vis.sum())) < 1e-13
+
+
+def test_identical_keys(oracle_mod):
+    P, T, H = 5, 3, 2
+    w = _tiny(H=H, T=T, prefix=(P,), seed=18, num_slots=32)
+    w.kv_pool[:] = w.kv_pool[3]
+    out, lse, _ = _run(oracle_mod, w)
+    q, kv = _np_inputs(w)
+    mask = _dense_mask(w.parents[0].tolist(), P)
+    for i in range(T):
+        for h in range(H):
+            s = w.spec.sm_scale * float(q[i, h] @ kv[3])
+            assert abs(lse[i * H + h] - (s + math.log(mask[i].sum()))) < 1e-12
+            np.testing.assert_allclose(out[i * H + h], kv[3, :512], rtol=0, atol=1e-12)
+
+
+def test_dominant_key(oracle_mod):
+    """One key whose scaled logit exceeds all others by > 50 takes all the weight."""
+    P, T, H = 8, 2, 1
+    w = _tiny(H=H, T=T, prefix=(P,), tree="chain", seed=19, num_slots=32)
+    w.q.zero_()
+    w.q[:, :, 0] = 4.0
+    w.kv_pool[:, 0] = 0.0
+    dom = int(w.slot_idx[3])
+    w.kv_pool[dom, 0] = 256.0        # logit gap = 4 * 256 / sqrt(192) ~ 73.9
+    out, lse, _ = _run(oracle_mod, w)
+    _, kv = _np_inputs(w)
+    for r in range(T * H):
+        np.testing.assert_allclose(out[r], kv[dom, :512], rtol=0, atol=1e-20 + 1e-25)
+        assert abs(lse[r] - 4.0 * 256.0 * w.spec.sm_scale) < 1e-12
+
+
+def test_scale_enters_linearly(oracle_mod):
+    """lse(scale=0) = ln|K|; and out depends on the scale (guards a dropped scale)."""
+    w = _tiny(H=1, T=2, prefix=(4,), tree="chain", seed=20, num_slots=32)
+    w.spec.sm_scale = 0.0
+    out0, lse0, _ = _run(oracle_mod, w)
+    np.testing.assert_allclose(lse0, [math.log(5), math.log(6)], atol=1e-15)
+    w.spec.sm_scale = 0.3
+    out1, _, _ = _run(oracle_mod, w)
+    assert np.abs(out1 - out0).max() > 1e-3
+
+
+# ------------------------------------------------------ skips and windows
+
+def test_out_of_range_slot_is_skipped(oracle_mod):
+    w = _tiny(H=2, T=2, prefix=(6,), tree="chain", seed=22, num_slots=32)
+    ref = _tiny(H=2, T=2, prefix=(5,), tree="chain", seed=22, num_slots=32)
+    ref.q, ref.kv_pool = w.q, w.kv_pool
+    ref.slot_idx = torch.cat([w.slot_idx[:2], w.slot_idx[3:]])
+    ref.kv_indptr = torch.tensor([0, 7], dtype=torch.int32)
+    w.slot_idx[2] = 32 + 5
+    out, lse, skipped = _run(oracle_mod, w)
+    assert skipped == 2 * 2          # every row of both nodes skips that prefix key
+    out_r, lse_r, _ = _run(oracle_mod, ref)
+    np.testing.assert_allclose(out, out_r, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_r, rtol=0, atol=1e-13)
+
+
+def test_row_subset_matches_full(oracle_mod):
+    w = _tiny(B=2, H=3, T=4, prefix=(7, 2), seed=23, num_slots=64)
+    out, lse, _ = _run(oracle_mod, w)
+    rows = [0, 5, 13, 23]
+    o2, l2, _ = _run(oracle_mod, w, rows=rows)
+    np.testing.assert_array_equal(o2, out[rows])
+    np.testing.assert_array_equal(l2, lse[rows])
+
+
+# ------------------------------------------------------------------ defrag
+
+def test_defrag_copies_rows_and_preserves_attention(oracle_mod):
+    # live rows in [0, 64) of a 128-row pool; destinations in the free upper half
+    w = _tiny(B=2, H=2, T=3, prefix=(5, 4), seed=24, num_slots=64)
+    w.kv_pool = torch.cat([w.kv_pool, synth._bf16_normal((64, 576), torch.Generator().manual_seed(9))])
+    out0, lse0, _ = _run(oracle_mod, w)
+    pool = synth.as_u16(w.kv_pool)
+    ip = w.kv_indptr.numpy().astype(np.int64)
+    dst = np.array([80, 100], dtype=np.int64)
+    src = w.slot_idx.numpy()
+    newpool, newslots = oracle_mod.defrag(pool, src, ip, dst)
+    touched = set()
+    for b in range(2):
+        for i in range(ip[b + 1] - ip[b]):
+            assert newslots[ip[b] + i] == dst[b] + i
+            np.testing.assert_array_equal(newpool[dst[b] + i], pool[src[ip[b] + i]])
+            touched.add(int(dst[b] + i))
+    for r in range(128):
+        if r not in touched:
+            np.testing.assert_array_equal(newpool[r], pool[r])
+    bits, _ = oracle_mod.tree_bits(w.parents.numpy())
+    out1, lse1, _ = oracle_mod.verify_attn(synth.as_u16(w.q), newpool, newslots, ip,
+                                           w.prefix_len.numpy(), bits, w.spec.sm_scale)
+    np.testing.assert_array_equal(out0, out1)
+    np.testing.assert_array_equal(lse0, lse1)
