@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of one MLA tree-verify attention step on GB300.
+
+Default workload: one request, H=8 heads, T=16 random draft-tree nodes,
+prefix 4096 keys, bf16 latent KV gathered through a page_size=1 slot table
+scattered over a 2^20-slot pool (the TP8 slice).  A step is one verify call:
+tree-mask evaluation, split-K partial attention and the LSE merge.
+
+Prints ONE JSON line: effective KV GB/s (whole job), us/step, the split-K
+kernel's roofline fraction, the oracle timed on the host cores, an
+end-to-end figure through the C ABI with host buffers, clocks and launches.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "verify-attn µs/step and effective KV GB/s (% of HBM roofline) vs prefix length"
+WORKLOAD = ("TP8 slice: 1 request, H=8, T=16 random tree, prefix 4096, bf16 latent KV "
+            "(576 = 512 + 64), page_size=1 slots scattered over a 2^20-slot pool, "
+            "sm_scale=1/sqrt(192)")
+SWEEP_P = [4096, 16384, 32768, 65536, 131072, 200000]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 FMA, 2 tensor cores")
+    ap.add_argument("--nsplit", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1 + 0.15):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------------- workload
+
+def device_pool(num_slots: int, seed: int, dev) -> torch.Tensor:
+    """The shared latent pool, drawn on the device (seeded) in chunks."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    pool = torch.empty(num_slots, synth.D_QK, dtype=torch.bfloat16, device=dev)
+    step = 1 << 17
+    for r0 in range(0, num_slots, step):
+        r1 = min(num_slots, r0 + step)
+        pool[r0:r1] = torch.randn(r1 - r0, synth.D_QK, generator=g, device=dev).to(torch.bfloat16)
+    return pool
+
+
+class Step:
+    """Device-resident inputs of one verify step plus `nrot` rotated slot tables
+    (disjoint random subsets of the pool) so that consecutive steps read rows
+    that are not in L2."""
+
+    def __init__(self, va, pool, H, T, P, seed, nrot, dev, path, nsplit):
+        self.va = va
+        self.pool = pool
+        self.H, self.T, self.P = H, T, P
+        self.N = P + T
+        g = torch.Generator().manual_seed(seed)
+        self.q = (torch.randn(T, H, synth.D_QK, generator=g)).to(torch.bfloat16).to(dev)
+        self.parents = synth.make_parents(T, "random", g).view(1, T).to(dev)
+        perm = torch.randperm(pool.shape[0], generator=g)
+        if nrot * self.N > pool.shape[0]:
+            nrot = max(1, pool.shape[0] // self.N)
+        self.nrot = nrot
+        self.tables = [perm[k * self.N:(k + 1) * self.N].to(torch.int32).to(dev)
+                       for k in range(nrot)]
+        self.indptr = torch.tensor([0, self.N], dtype=torch.int32, device=dev)
+        self.prefix = torch.tensor([P], dtype=torch.int32, device=dev)
+        self.path = path
+        self.ws, self.nsplit = va.alloc_workspace(1, T, H, nsplit, path, dev)
+        self.out = torch.empty(T, H, synth.D_V, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+        self.kv_bytes = self.N * synth.D_QK * 2
+
+    def call(self, k, stream=None):
+        self.va.verify_attn_paged(self.q, self.pool, self.tables[k % self.nrot], self.indptr,
+                                  self.prefix, self.parents, sm_scale=synth.SM_SCALE,
+                                  nsplit=self.nsplit, flags=self.path, workspace=self.ws,
+                                  out=self.out, lse=self.lse, stream=stream)
+
+
+def capture_graphs(step: Step, with_events: bool):
+    """One CUDA graph per rotated slot table; optionally with event records
+    around the split-K kernel inside each graph."""
+    va = step.va
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for k in range(min(step.nrot, 3)):
+            step.call(k)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graphs, evs = [], []
+    for k in range(step.nrot):
+        g = torch.cuda.CUDAGraph()
+        if with_events:
+            eb = torch.cuda.Event(enable_timing=True)
+            ea = torch.cuda.Event(enable_timing=True)
+            va.set_partial_events(eb, ea)
+            evs.append((eb, ea))
+        with torch.cuda.graph(g):
+            step.call(k)
+        graphs.append(g)
+    va.set_partial_events(None, None)
+    return graphs, evs
+
+
+def time_graphs(graphs, K, W, dist=None):
+    for k in range(W):
+        graphs[k % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(K):
+        graphs[k % len(graphs)].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_ms(evs, used):
+    """Average split-K kernel duration over the last replay of each graph used."""
+    n = min(len(evs), used)
+    return float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in range(n)]))
+
+
+def check_parity(step: Step, k: int, nrows: int = 8):
+    """Sampled rows of step k against the fp64 oracle (compact copy of the rows used)."""
+    import oracle
+    step.call(k)
+    torch.cuda.synchronize()
+    table = step.tables[k % step.nrot].long()
+    rows_kv = step.pool[table].cpu()
+    rng = np.random.default_rng(k)
+    rows = np.sort(rng.choice(step.T * step.H, size=min(nrows, step.T * step.H), replace=False))
+    bits, _ = oracle.tree_bits(step.parents.cpu().numpy())
+    ro, rl, _ = oracle.verify_attn(synth.as_u16(step.q.cpu()), synth.as_u16(rows_kv),
+                                   np.arange(step.N, dtype=np.int32), np.array([0, step.N]),
+                                   np.array([step.P]), bits, synth.SM_SCALE, rows=rows)
+    go = step.out.float().reshape(-1, 512).cpu().numpy()[rows]
+    gl = step.lse.reshape(-1).cpu().numpy()[rows]
+    err = float(np.abs(go - ro).max())
+    mean = float(np.abs(go - ro).mean())
+    lerr = float(np.abs(gl - rl).max())
+    return {"rows": int(len(rows)), "max_abs": err, "mean_abs": mean, "lse_max_abs": lerr,
+            "ok": bool(err <= 2e-2 and mean <= 2e-3 and lerr <= 1e-3)}
+
+
+# --------------------------------------------------------------- oracle
+
+def cpu_oracle(P, H, T, seed, budget_s=12.0, threads=None):
+    """The fp64 oracle on whole steps of the same workload until ~budget_s."""
+    import oracle
+    threads = threads or oracle.default_threads()
+    g = torch.Generator().manual_seed(seed)
+    N = P + T
+    q = synth.as_u16(torch.randn(T, H, synth.D_QK, generator=g).to(torch.bfloat16))
+    kv = synth.as_u16(torch.randn(N, synth.D_QK, generator=g).to(torch.bfloat16))
+    parents = synth.make_parents(T, "random", g).view(1, T).numpy()
+    bits, _ = oracle.tree_bits(parents)
+    slots = np.random.default_rng(seed).permutation(N).astype(np.int32)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        oracle.verify_attn(q, kv, slots, np.array([0, N]), np.array([P]), bits, synth.SM_SCALE,
+                           threads=threads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or steps >= 1000:
+            break
+    per = el / steps
+    return {"value": N * synth.D_QK * 2 / per / 1e9, "unit": "GB/s", "cores": int(threads),
+            "kind": "oracle", "us_per_step": per * 1e6,
+            "sample": f"{steps} whole step(s) of the same shape (P={P}, H={H}, T={T}), "
+                      f"fp64, {el:.1f} s"}
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    P, H, T = 4096, 8, 16
+    g = torch.Generator().manual_seed(1)
+    N = P + T
+    q = synth.as_u16(torch.randn(T, H, synth.D_QK, generator=g).to(torch.bfloat16))
+    kv = synth.as_u16(torch.randn(N, synth.D_QK, generator=g).to(torch.bfloat16))
+    parents = synth.make_parents(T, "random", g).view(1, T).numpy()
+    slots = np.random.default_rng(1).permutation(N).astype(np.int32)
+
+    def one():
+        bits, _ = oracle.tree_bits(parents)
+        oracle.verify_attn(q, kv, slots, np.array([0, N]), np.array([P]), bits, synth.SM_SCALE,
+                           threads=threads)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    val = N * synth.D_QK * 2 / (ms / 1e3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD + " (each step: the whole step on the host cores)"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{args.steps} whole steps"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        dist = tdist
+    import mla_speculative_decode_gb300 as va
+    va.build()
+    va.init(local)
+    hbm_peak, tc_peak, peak_kind = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    # ---- headline workload
+    H, T, P = 8, 16, 4096
+    pool = device_pool(1 << 20, seed=1 + rank, dev=dev)
+    kv_step = (P + T) * synth.D_QK * 2
+    nrot = max(2, math.ceil(3 * l2 / kv_step))
+    step = Step(va, pool, H, T, P, seed=1 + rank, nrot=nrot, dev=dev, path=args.path,
+                nsplit=args.nsplit)
+    parity = check_parity(step, 0)
+    graphs, evs = capture_graphs(step, with_events=True)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    ms = time_graphs(graphs, args.steps, args.warmup, dist)
+    t_wall1 = time.time()
+    k_ms = kernel_ms(evs, args.steps)
+    time.sleep(0.25)
+    clocks.stop()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * kv_step * args.steps / (ms / 1e3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if True:
+        pin = lambda t: t.cpu().pin_memory()
+        hq, hpar, hind, hpre = pin(step.q), pin(step.parents), pin(step.indptr), pin(step.prefix)
+        htabs = [pin(t) for t in step.tables]
+        ho = torch.empty_like(step.out, device="cpu").pin_memory()
+        hl = torch.empty_like(step.lse, device="cpu").pin_memory()
+        dq, dpar = torch.empty_like(step.q), torch.empty_like(step.parents)
+        dind, dpre = torch.empty_like(step.indptr), torch.empty_like(step.prefix)
+        dtab = torch.empty_like(step.tables[0])
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hpar, hind, hpre, htabs[0]))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        Ke = min(args.steps, 500)
+
+        def e2e_step(k):
+            dq.copy_(hq, non_blocking=True)
+            dpar.copy_(hpar, non_blocking=True)
+            dind.copy_(hind, non_blocking=True)
+            dpre.copy_(hpre, non_blocking=True)
+            dtab.copy_(htabs[k % len(htabs)], non_blocking=True)
+            va.verify_attn_paged(dq, step.pool, dtab, dind, dpre, dpar, sm_scale=synth.SM_SCALE,
+                                 nsplit=step.nsplit, flags=step.path, workspace=step.ws,
+                                 out=step.out, lse=step.lse)
+            ho.copy_(step.out, non_blocking=True)
+            hl.copy_(step.lse, non_blocking=True)
+
+        for k in range(min(args.warmup, 20)):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in range(Ke):
+            e2e_step(k)
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / Ke
+        e2e = {"value": world * kv_step / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "us_per_step": e_ms * 1e3, "steps": Ke, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    # ---- prefix sweeps (H=8 and H=64, T=16), scattered slots
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for Hs in (8, 64):
+            for Ps in SWEEP_P:
+                kvb = (Ps + 16) * synth.D_QK * 2
+                nr = max(1, min(16, math.ceil(3 * l2 / kvb)))
+                st = Step(va, pool, Hs, 16, Ps, seed=7, nrot=nr, dev=dev, path=args.path,
+                          nsplit=0)
+                gs, ev = capture_graphs(st, with_events=True)
+                reps = max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8))))
+                tms = time_graphs(gs, reps, 5)
+                kms = kernel_ms(ev, reps)
+                us = tms / reps * 1e3
+                sweep.append({"H": Hs, "T": 16, "P": Ps, "us_per_step": us,
+                              "gbs": kvb / (us * 1e-6) / 1e9,
+                              "frac_hbm": kvb / (us * 1e-6) / 1e9 / hbm_peak,
+                              "partial_kernel_us": kms * 1e3,
+                              "partial_gbs": kvb / (kms * 1e-3) / 1e9, "nsplit": st.nsplit,
+                              "path": "auto" if args.path == 0 else str(args.path)})
+                del gs, ev, st
+                torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_oracle(P, H, T, seed=1)
+
+    clk = clocks.summary(t_wall0, t_wall1) or clocks.summary()
+    achieved = kv_step / (k_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q and KV, random trees, random slot scatter)",
+        "config": {"workload": WORKLOAD, "B": 1, "H": H, "T": T, "prefix": P,
+                   "kv_bytes_per_step": kv_step, "nsplit": step.nsplit,
+                   "path": ["auto", "fma", "tc"][args.path],
+                   "l2": f"inputs larger than L2: {step.nrot} rotating slot tables "
+                         f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
+                   "launch": "CUDA graph per step", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "split-K partial", "kernel_us": k_ms * 1e3,
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk,
+        "parity": parity, "sweep": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * verify_attn.h -- C ABI of the GB300 (sm_103a) MLA tree-verify attention library.
+ *
+ * The operation (The Milestone Commit, "Input Knowledge Required"): in tree
+ * speculative decoding the target model verifies T draft-tree tokens in one
+ * pass; each token's H absorbed query heads attend over the request's whole
+ * cached KV.  The cache is the MLA latent cache (The Milestone Commit,
+ * "Context"): one row per token, shared by every head, addressed through a
+ * page_size=1 slot table.  A row holds 576 bf16: 512 latent columns, which
+ * are also the value, followed by 64 rotary columns.  The Checkpoint Report,
+ * "Mistakes and Incorrect Assumptions": the request's keys are its prefix
+ * followed by the draft tokens' own keys, and draft node i sees every prefix
+ * key plus the draft keys of itself and its ancestors.
+ *
+ * For request b, node i, head h (row r = (b*T + i)*H + h):
+ *   s_j   = sm_scale * <q[r, 0:576], kv[slot(b, j), 0:576]>   for visible j
+ *   lse_r = ln sum_j exp(s_j)                 (natural log, scale included)
+ *   out_r = sum_j exp(s_j - lse_r) * kv[slot(b, j), 0:512]
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises inside a call, and launches only
+ *    on the caller's stream, so every call can be captured into a CUDA graph
+ *    (The Commit That Locked In 6x Decode, "1. Capture-Safe Design": no
+ *    cudaMalloc and no host sync inside the call; a workspace allocated once
+ *    by the caller).
+ *  - Step-varying data (prefix lengths, slot tables, tree parents) is read on
+ *    the device, so one captured graph replays across decode steps.
+ *  - Host-checkable argument errors return a negative VA_ERR_* code before any
+ *    device work is enqueued.  Device-data errors (a slot outside the pool, a
+ *    parent that is not an earlier node, a slot list shorter than
+ *    prefix_len + T) set bits in the workspace status word; the offending key
+ *    is skipped and the call still returns VA_OK.  Kernels never trap.
+ *  - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
+ *  - Calls on distinct workspaces are thread-safe.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *va_stream_t;
+
+/* Return codes of every entry point. */
+#define VA_OK               0
+#define VA_ERR_NULL        -1  /* a required pointer is NULL                        */
+#define VA_ERR_SHAPE       -2  /* B, T, H, num_slots, stride or nsplit out of range */
+#define VA_ERR_ALIGN       -3  /* pointer or stride misaligned (see each argument)  */
+#define VA_ERR_WORKSPACE   -4  /* workspace smaller than va_workspace_bytes()       */
+#define VA_ERR_UNSUPPORTED -5  /* no va_init() for the current device, device is
+                                  not sm_103, or the requested path is unavailable */
+#define VA_ERR_LAUNCH      -6  /* a kernel launch failed (cudaGetLastError)         */
+#define VA_ERR_CUDA        -7  /* another CUDA runtime call failed                  */
+
+/* Bits of the device status word (first 4 bytes of the workspace). */
+#define VA_STATUS_BAD_SLOT    0x1u  /* a slot index outside [0, num_slots)           */
+#define VA_STATUS_BAD_PARENT  0x2u  /* parent[i] not in [-1, i); node treated as a
+                                       child of the prefix                          */
+#define VA_STATUS_BAD_INDPTR  0x4u  /* slot list of a request shorter than
+                                       prefix_len + T, or prefix_len < 0; the
+                                       request's prefix is clamped to what exists  */
+#define VA_STATUS_TIMEOUT     0x8u  /* a bounded device-side wait gave up            */
+#define VA_STATUS_BAD_DST     0x10u /* defrag destination outside the pool           */
+
+/* Fixed widths of the MLA latent row. */
+#define VA_D_QK 576   /* key / query width: 512 latent + 64 rotary */
+#define VA_D_V  512   /* value / output width: the first 512 columns */
+#define VA_T_MAX 64   /* draft nodes per request (one 64-bit mask word per node) */
+#define VA_NSPLIT_MAX 1024
+
+/* Compute-path selection for the verify entry points (`flags`). */
+#define VA_PATH_AUTO 0  /* library's choice                                     */
+#define VA_PATH_FMA  1  /* CUDA-core FMA path (any shape)                       */
+#define VA_PATH_TC   2  /* tcgen05 tensor-core path                             */
+
+/* Library ABI version (major * 100 + minor). */
+int va_version(void);
+
+/*
+ * Caches the device's SM count and checks that it is an sm_103 part.  Call
+ * once per device, outside stream capture, before the first verify call on
+ * that device.  Returns VA_OK, VA_ERR_UNSUPPORTED or VA_ERR_CUDA.
+ */
+int va_init(int device);
+
+/*
+ * Split count the library picks for nsplit = 0 on the current device (after
+ * va_init): enough (request, row-block, split) work items to cover the SMs.
+ * Pure host arithmetic.  Returns >= 1, or a VA_ERR_* code.
+ */
+int va_auto_nsplit(int B, int T, int H, int flags);
+
+/*
+ * Bytes of workspace a verify call with these sizes needs (nsplit >= 1; pass
+ * the value from va_auto_nsplit for automatic splitting).  Pure host
+ * arithmetic, no CUDA call.  Layout (each region 256-byte aligned):
+ *   [0, 256)        status word (uint32) and reserved header
+ *   tree masks      uint64 [B*T]
+ *   partial lse     float  [nsplit][B*T*H]
+ *   partial out     float  [nsplit][B*T*H][512]
+ * The Commit That Locked In 6x Decode, "Input Knowledge Required" (NSPLIT and
+ * partial-reduce: each split writes a partial result that a reduction merges).
+ */
+size_t va_workspace_bytes(int B, int T, int H, int nsplit);
+
+/*
+ * Paged verify attention: keys gathered through a page_size=1 slot table.
+ *   q             bf16 [B*T, H, 576], contiguous, 16-byte aligned.
+ *   kv_pool       bf16 [num_slots, kv_row_stride]; row stride in elements,
+ *                 >= 576 and a multiple of 8; base 16-byte aligned.  Only the
+ *                 first 576 columns of a row are read.
+ *   slot_idx      int32, request b's N_b = prefix_len[b] + T slots start at
+ *                 slot_idx[kv_indptr[b]]: the prefix slots in order, then the
+ *                 slots of draft nodes 0..T-1 (The Checkpoint Report,
+ *                 "Mistakes and Incorrect Assumptions": prefix in kv_indices,
+ *                 draft tokens at out_cache_loc -- concatenated here).
+ *   kv_indptr     int32 [B+1] device offsets into slot_idx.
+ *   prefix_len    int32 [B] device, keys before the draft nodes (>= 0).
+ *   tree_parent   int32 [B, T] device, parent[i] in [-1, i); -1 = the node
+ *                 hangs off the prefix.  May be NULL when tree_bits is given.
+ *   tree_bits     uint64 [B, T] device, bit k of tree_bits[b*T+i] set when
+ *                 draft node k is node i or one of its ancestors.  When
+ *                 non-NULL it is used and tree_parent is ignored.
+ *   B, T, H       1 <= B, 1 <= T <= 64, 1 <= H.
+ *   sm_scale      scale applied to the 576-wide dot product.
+ *   nsplit        key-range splits per (request, row block); 0 = automatic
+ *                 (The Commit That Locked In 6x Decode, "2. NSPLIT=64 for TP8
+ *                 Occupancy").  Splits that would hold fewer than 64 keys are
+ *                 dropped on the device from the actual prefix length.
+ *   flags         VA_PATH_*.
+ *   workspace     device buffer of workspace_bytes >= va_workspace_bytes(B, T,
+ *                 H, nsplit or the automatic value), 256-byte aligned, owned
+ *                 by the caller; reused across calls; calls that overlap on
+ *                 the device must not share one.
+ *   out           bf16 [B*T, H, 512], 16-byte aligned (round-to-nearest-even).
+ *   lse           float [B*T, H]; -inf for a row that sees no key.
+ *   stream        stream the kernels are launched on.
+ * The status word is cleared by the call itself before any check runs.
+ */
+int verify_attn_paged(const void *q, const void *kv_pool, int64_t num_slots,
+                      int64_t kv_row_stride, const int32_t *slot_idx, const int32_t *kv_indptr,
+                      const int32_t *prefix_len, const int32_t *tree_parent,
+                      const uint64_t *tree_bits, int B, int T, int H, float sm_scale, int nsplit,
+                      int flags, void *workspace, size_t workspace_bytes, void *out, float *lse,
+                      va_stream_t stream);
+
+/*
+ * Contiguous verify attention: request b's N_b = prefix_len[b] + T keys are
+ * the pool rows kv_start[b] + j, j < N_b (prefix rows first, then the draft
+ * nodes' rows) -- the layout after defragmentation (The Checkpoint Report,
+ * "Input Knowledge Required": defragmentation keeps per-request KV
+ * contiguous; The Milestone Commit, "What the Commit Captures": the first
+ * kernel read contiguous KV).  kv_start is int64 [B] on the device; rows
+ * outside [0, num_slots) are skipped and flagged VA_STATUS_BAD_SLOT.  Every
+ * other argument is as for verify_attn_paged.
+ */
+int verify_attn_contiguous(const void *q, const void *kv_pool, int64_t num_slots,
+                           int64_t kv_row_stride, const int64_t *kv_start,
+                           const int32_t *prefix_len, const int32_t *tree_parent,
+                           const uint64_t *tree_bits, int B, int T, int H, float sm_scale,
+                           int nsplit, int flags, void *workspace, size_t workspace_bytes,
+                           void *out, float *lse, va_stream_t stream);
+
+/*
+ * KV defragmentation (The Checkpoint Report, "Input Knowledge Required" and
+ * "The Architecture of the Report": the deferred defragmentation phase).
+ * For every request b and i < n_b = src_indptr[b+1] - src_indptr[b]:
+ *   kv_pool[dst_base[b] + i, :] <- kv_pool[src_slots[src_indptr[b] + i], :]
+ * copying whole rows (kv_row_stride elements), and, when slot_idx_out is not
+ * NULL, slot_idx_out[src_indptr[b] + i] <- dst_base[b] + i.
+ *   src_slots    int32 device; src_indptr int32 [B+1] device; dst_base int64
+ *                [B] device.  slot_idx_out may alias src_slots.
+ *   max_rows     host upper bound on sum_b n_b, used only to size the grid
+ *                (any value >= 1 is correct; larger gives more parallelism).
+ *   status       optional device uint32 word; bits VA_STATUS_BAD_SLOT /
+ *                VA_STATUS_BAD_DST are OR-ed in for rows that are skipped.
+ * The destination ranges must not overlap any source row of the same call;
+ * rows are copied by independent threads, so an overlap gives an undefined
+ * result (never a fault: every address is range-checked).
+ */
+int verify_attn_defrag(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
+                       const int32_t *src_slots, const int32_t *src_indptr,
+                       const int64_t *dst_base, int32_t *slot_idx_out, int B, int64_t max_rows,
+                       uint32_t *status, va_stream_t stream);
+
+/*
+ * Benchmark helper: while both handles are non-NULL, every verify call on this
+ * process records cudaEvent_t `before` on its stream immediately before it
+ * launches the split-K partial kernel and `after` immediately after, so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  Pass NULLs to
+ * stop.  Process-wide setting, not thread-safe; the events must belong to the
+ * device of the calls.  Recording is a stream operation, so it is captured
+ * into a graph like the kernels are.  Returns VA_OK.
+ */
+int va_set_partial_events(void *before, void *after);
+
+/*
+ * Test helper: waits for `stream`, then copies the workspace status word to
+ * *status_host.  This one call synchronises; do not use it inside capture.
+ */
+int va_read_status(const void *workspace, uint32_t *status_host, va_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

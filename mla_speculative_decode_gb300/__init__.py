@@ -1,0 +1,265 @@
+"""Python binding of libverifyattn.so -- GB300 (sm_103a) MLA tree-verify attention.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/verify_attn.h``.  PyTorch
+provides device memory and streams.  There is no CPU fallback: if the shared
+library has not been built, :func:`load` raises.
+
+Names follow the C ABI: ``verify_attn_paged``, ``verify_attn_contiguous``,
+``verify_attn_defrag``, ``workspace_bytes``, ``auto_nsplit``, ``init``,
+``read_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import _builder as _build_mod
+
+D_QK = 576
+D_V = 512
+T_MAX = 64
+
+VA_OK = 0
+ERRORS = {-1: "VA_ERR_NULL", -2: "VA_ERR_SHAPE", -3: "VA_ERR_ALIGN", -4: "VA_ERR_WORKSPACE",
+          -5: "VA_ERR_UNSUPPORTED", -6: "VA_ERR_LAUNCH", -7: "VA_ERR_CUDA"}
+STATUS_BAD_SLOT = 0x1
+STATUS_BAD_PARENT = 0x2
+STATUS_BAD_INDPTR = 0x4
+STATUS_TIMEOUT = 0x8
+STATUS_BAD_DST = 0x10
+PATH_AUTO, PATH_FMA, PATH_TC = 0, 1, 2
+
+LIB_PATH = _build_mod.LIB
+
+
+class VaError(RuntimeError):
+    def __init__(self, func: str, code: int):
+        self.code = code
+        super().__init__(f"{func} returned {code} ({ERRORS.get(code, 'unknown')})")
+
+
+_lib = None
+_inited = set()
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA sources into libverifyattn.so (nvcc, sm_103a)."""
+    return _build_mod.build(force=force)
+
+
+def load() -> ctypes.CDLL:
+    """Load libverifyattn.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libverifyattn.so is not built ({LIB_PATH}); run "
+                           "mla_speculative_decode_gb300.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.va_version.argtypes = []
+    lib.va_version.restype = i32
+    lib.va_init.argtypes = [i32]
+    lib.va_init.restype = i32
+    lib.va_auto_nsplit.argtypes = [i32, i32, i32, i32]
+    lib.va_auto_nsplit.restype = i32
+    lib.va_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.va_workspace_bytes.restype = sz
+    lib.verify_attn_paged.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32, i32, i32,
+                                      P, sz, P, P, P]
+    lib.verify_attn_paged.restype = i32
+    lib.verify_attn_contiguous.argtypes = [P, P, i64, i64, P, P, P, P, i32, i32, i32, f32, i32, i32,
+                                           P, sz, P, P, P]
+    lib.verify_attn_contiguous.restype = i32
+    lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
+    lib.verify_attn_defrag.restype = i32
+    lib.va_set_partial_events.argtypes = [P, P]
+    lib.va_set_partial_events.restype = i32
+    lib.va_read_status.argtypes = [P, P, P]
+    lib.va_read_status.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(func: str, rc: int) -> int:
+    if rc < 0:
+        raise VaError(func, rc)
+    return rc
+
+
+def init(device: Optional[int] = None) -> None:
+    """va_init for `device` (default: torch's current device); idempotent."""
+    if device is None:
+        device = torch.cuda.current_device()
+    if device in _inited:
+        return
+    _check("va_init", load().va_init(int(device)))
+    _inited.add(device)
+
+
+def workspace_bytes(B: int, T: int, H: int, nsplit: int) -> int:
+    n = load().va_workspace_bytes(B, T, H, nsplit)
+    if n == 0:
+        raise VaError("va_workspace_bytes", -2)
+    return n
+
+
+def auto_nsplit(B: int, T: int, H: int, flags: int = PATH_AUTO) -> int:
+    init()
+    return _check("va_auto_nsplit", load().va_auto_nsplit(B, T, H, flags))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, name: str, dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def alloc_workspace(B: int, T: int, H: int, nsplit: int = 0, flags: int = PATH_AUTO,
+                    device=None) -> Tuple[torch.Tensor, int]:
+    """A workspace tensor for these sizes and the nsplit it was sized for."""
+    ns = nsplit if nsplit > 0 else auto_nsplit(B, T, H, flags)
+    n = workspace_bytes(B, T, H, ns)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda"), ns
+
+
+def _outputs(rows: int, H: int, device, out, lse):
+    if out is None:
+        out = torch.empty(rows, H, D_V, dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty(rows, H, dtype=torch.float32, device=device)
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    return out, lse
+
+
+def _tree_args(tree_parent, tree_bits):
+    if tree_bits is not None:
+        _dev(tree_bits, "tree_bits", torch.int64)
+    elif tree_parent is not None:
+        _dev(tree_parent, "tree_parent", torch.int32)
+    return _ptr(tree_parent), _ptr(tree_bits)
+
+
+def verify_attn_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor,
+                      kv_indptr: torch.Tensor, prefix_len: torch.Tensor,
+                      tree_parent: Optional[torch.Tensor] = None,
+                      tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                      nsplit: int = 0, flags: int = PATH_AUTO,
+                      workspace: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA tree-verify attention; returns (out bf16 [B*T, H, 512], lse fp32 [B*T, H]).
+
+    q [B*T, H, 576] bf16; kv_pool [num_slots, stride] bf16; slot_idx int32;
+    kv_indptr int32 [B+1]; prefix_len int32 [B]; tree_parent int32 [B, T] or
+    tree_bits int64 [B, T] (bit patterns of uint64 masks).  All CUDA tensors.
+    """
+    init(q.device.index)
+    _dev(q, "q", torch.bfloat16)
+    _dev(kv_pool, "kv_pool", torch.bfloat16)
+    _dev(slot_idx, "slot_idx", torch.int32)
+    _dev(kv_indptr, "kv_indptr", torch.int32)
+    _dev(prefix_len, "prefix_len", torch.int32)
+    if q.dim() != 3 or q.shape[2] != D_QK or kv_pool.dim() != 2:
+        raise ValueError("q must be [B*T, H, 576] and kv_pool [num_slots, stride]")
+    B = prefix_len.shape[0]
+    T = q.shape[0] // B
+    H = q.shape[1]
+    if workspace is None:
+        workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
+    out, lse = _outputs(q.shape[0], H, q.device, out, lse)
+    par, bits = _tree_args(tree_parent, tree_bits)
+    rc = load().verify_attn_paged(
+        _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
+        _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,
+        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
+    _check("verify_attn_paged", rc)
+    return out, lse
+
+
+def verify_attn_contiguous(q: torch.Tensor, kv_pool: torch.Tensor, kv_start: torch.Tensor,
+                           prefix_len: torch.Tensor, tree_parent: Optional[torch.Tensor] = None,
+                           tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                           nsplit: int = 0, flags: int = PATH_AUTO,
+                           workspace: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Contiguous-KV variant: request b's keys are pool rows kv_start[b] + j (int64 [B])."""
+    init(q.device.index)
+    _dev(q, "q", torch.bfloat16)
+    _dev(kv_pool, "kv_pool", torch.bfloat16)
+    _dev(kv_start, "kv_start", torch.int64)
+    _dev(prefix_len, "prefix_len", torch.int32)
+    B = prefix_len.shape[0]
+    T = q.shape[0] // B
+    H = q.shape[1]
+    if workspace is None:
+        workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
+    out, lse = _outputs(q.shape[0], H, q.device, out, lse)
+    par, bits = _tree_args(tree_parent, tree_bits)
+    rc = load().verify_attn_contiguous(
+        _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_start),
+        _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags, _ptr(workspace),
+        workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
+    _check("verify_attn_contiguous", rc)
+    return out, lse
+
+
+def verify_attn_defrag(kv_pool: torch.Tensor, src_slots: torch.Tensor, src_indptr: torch.Tensor,
+                       dst_base: torch.Tensor, slot_idx_out: Optional[torch.Tensor] = None,
+                       max_rows: Optional[int] = None, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """Copy request b's rows src_slots[indptr[b]:indptr[b+1]] to dst_base[b] + i (in place)."""
+    init(kv_pool.device.index)
+    _dev(kv_pool, "kv_pool", torch.bfloat16)
+    _dev(src_slots, "src_slots", torch.int32)
+    _dev(src_indptr, "src_indptr", torch.int32)
+    _dev(dst_base, "dst_base", torch.int64)
+    if slot_idx_out is not None:
+        _dev(slot_idx_out, "slot_idx_out", torch.int32)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    B = dst_base.shape[0]
+    rows = int(max_rows) if max_rows is not None else max(1, src_slots.numel())
+    rc = load().verify_attn_defrag(
+        _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(src_slots), _ptr(src_indptr),
+        _ptr(dst_base), _ptr(slot_idx_out), B, rows, _ptr(status), _stream(stream))
+    _check("verify_attn_defrag", rc)
+
+
+def read_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the workspace status word."""
+    v = ctypes.c_uint32(0)
+    _check("va_read_status", load().va_read_status(_ptr(workspace), ctypes.byref(v),
+                                                   _stream(stream)))
+    return int(v.value)
+
+
+def set_partial_events(before=None, after=None) -> None:
+    """Record torch.cuda.Event `before`/`after` around the split-K partial kernel
+    of every following verify call (None, None stops)."""
+    if before is None or after is None:
+        load().va_set_partial_events(None, None)
+        return
+    for e in (before, after):
+        if e.cuda_event == 0:
+            e.record()          # the handle is created on first record
+    load().va_set_partial_events(before.cuda_event, after.cuda_event)

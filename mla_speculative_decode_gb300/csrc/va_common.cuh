@@ -1,0 +1,159 @@
+// va_common.cuh -- definitions shared by the verify-attention kernels and the
+// host launcher: launch parameters, workspace layout, the split schedule and
+// small device helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "verify_attn.h"
+
+namespace va {
+
+constexpr int kDqk = VA_D_QK;   // 576: latent 512 + rotary 64
+constexpr int kDv = VA_D_V;     // 512
+constexpr int kTmax = VA_T_MAX;
+// Splits are cut on multiples of this many keys, so a split never holds a
+// ragged tile except at the request's end.
+constexpr int kSplitGrain = 64;
+constexpr size_t kHeaderBytes = 256;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Workspace regions (byte offsets from the workspace base).
+struct WsLayout {
+  size_t bits;   // uint64 [B*T]
+  size_t plse;   // float  [nsplit][rows]
+  size_t po;     // float  [nsplit][rows][512]
+  size_t total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int B, int T, int H, int nsplit) {
+  WsLayout L;
+  const size_t rows = size_t(B) * T * H;
+  L.bits = kHeaderBytes;
+  L.plse = L.bits + align256(size_t(B) * T * sizeof(uint64_t));
+  L.po = L.plse + align256(size_t(nsplit) * rows * sizeof(float));
+  L.total = L.po + align256(size_t(nsplit) * rows * kDv * sizeof(float));
+  return L;
+}
+
+// Everything a verify launch needs (passed by value to every kernel).
+struct Params {
+  const __nv_bfloat16* q;      // [B*T, H, 576]
+  const __nv_bfloat16* kv;     // [num_slots, kv_stride]
+  int64_t num_slots;
+  int64_t kv_stride;           // elements
+  const int32_t* slot_idx;     // paged: concatenated slot lists
+  const int32_t* kv_indptr;    // paged: [B+1]
+  const int64_t* kv_start;     // contiguous: [B] (NULL when paged)
+  const int32_t* prefix_len;   // [B]
+  const int32_t* tree_parent;  // [B, T] or NULL
+  const uint64_t* bits;        // [B, T] ancestor-or-self masks (caller's or workspace)
+  int B, T, H;
+  int rows_per_req;            // T * H
+  int nsplit;                  // splits per (request, row block) grid slot
+  float sm_scale;
+  float scale_log2;            // sm_scale * log2(e)
+  float* part_lse;             // [nsplit][rows]
+  float* part_o;               // [nsplit][rows][512]
+  uint32_t* status;
+  __nv_bfloat16* out;          // [rows, 512]
+  float* lse;                  // [rows]
+};
+
+// Key range of one split.  A request has N = prefix + T keys; it is cut into
+// at most `nsplit` pieces of a whole number of 64-key grains, so a short
+// request uses fewer splits (empty splits exit at once and the merge reads
+// only the first `nsplit_eff`).
+struct SplitRange {
+  int k0, k1, nsplit_eff;
+};
+
+__host__ __device__ inline SplitRange split_range(int N, int nsplit, int s) {
+  SplitRange r;
+  int grains = ceil_div(N > 0 ? N : 1, kSplitGrain);
+  int ne = nsplit < grains ? nsplit : grains;
+  if (ne < 1) ne = 1;
+  int chunk = ceil_div(grains, ne) * kSplitGrain;
+  ne = ceil_div(N > 0 ? N : 1, chunk);
+  r.nsplit_eff = ne;
+  r.k0 = s * chunk;
+  r.k1 = r.k0 + chunk < N ? r.k0 + chunk : N;
+  return r;
+}
+
+// Per-request key bookkeeping read on the device.
+struct ReqInfo {
+  int P;        // effective prefix length
+  int N;        // P + T
+  int nlist;    // keys that have a slot (paged: slot list length; contiguous: N)
+  int64_t base; // paged: offset into slot_idx; contiguous: first pool row
+};
+
+__device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
+  ReqInfo r;
+  int P = p.prefix_len[b];
+  bool bad = false;
+  if (P < 0) { P = 0; bad = true; }
+  if (p.kv_start == nullptr) {
+    int i0 = p.kv_indptr[b], i1 = p.kv_indptr[b + 1];
+    int nl = i1 - i0;
+    if (nl < 0) nl = 0;
+    if (nl < P + p.T) {
+      bad = true;
+      P = nl - p.T > 0 ? (nl - p.T < P ? nl - p.T : P) : 0;
+    }
+    r.nlist = nl;
+    r.base = i0;
+  } else {
+    r.base = p.kv_start[b];
+    r.nlist = P + p.T;
+  }
+  r.P = P;
+  r.N = P + p.T;
+  if (bad && flag) atomicOr(p.status, VA_STATUS_BAD_INDPTR);
+  return r;
+}
+
+// Pool row of key j of a request, or -1 when the key has no valid row.
+__device__ inline int64_t key_row(const Params& p, const ReqInfo& r, int j) {
+  if (j >= r.nlist) return -1;
+  int64_t s = p.kv_start ? r.base + j : int64_t(p.slot_idx[r.base + j]);
+  return (s >= 0 && s < p.num_slots) ? s : -1;
+}
+
+// Is key j visible to draft node i of request b?  (prefix: always; draft key
+// k = j - P: when bit k of node i's ancestor-or-self mask is set.)
+__device__ inline bool key_visible(const Params& p, const ReqInfo& r, int b, int i, int j) {
+  if (j < r.P) return true;
+  int k = j - r.P;
+  if (k >= p.T) return false;
+  return (p.bits[size_t(b) * p.T + i] >> k) & 1ull;
+}
+
+__device__ inline float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ inline float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ inline uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_tree_bits(const Params& p, uint64_t* bits_out, cudaStream_t st);
+cudaError_t launch_partial_fma(const Params& p, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const Params& p, cudaStream_t st);
+cudaError_t launch_defrag(void* pool, int64_t num_slots, int64_t stride, const int32_t* src,
+                          const int32_t* indptr, const int64_t* dst_base, int32_t* slots_out,
+                          int B, int64_t max_rows, uint32_t* status, cudaStream_t st);
+
+// Rows handled by one CTA of the FMA partial kernel.
+constexpr int kFmaRows = 16;
+
+}  // namespace va

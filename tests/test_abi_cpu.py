@@ -1,0 +1,139 @@
+"""The C ABI on a machine without a GPU: the library builds and loads, exports
+every function include/verify_attn.h declares, sizes workspaces on the host,
+and rejects bad arguments with its error codes before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_speculative_decode_gb300 as va
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "verify_attn.h")
+
+# fake, never dereferenced: the host checks run before any device access
+A16 = 0x10000
+A256 = 0x20000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    va.build()
+    return va.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("verify_attn_paged", "verify_attn_contiguous", "verify_attn_defrag",
+              "va_workspace_bytes", "va_init", "va_read_status", "va_auto_nsplit", "va_version",
+              "va_set_partial_events"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_exports_nothing_else():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", va.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in syms if s.startswith(("va_", "verify_attn"))}
+    assert ours == set(declared_functions())
+
+
+def test_version(lib):
+    assert lib.va_version() == 100
+
+
+def test_workspace_bytes_layout(lib):
+    B, T, H, ns = 2, 16, 8, 5
+    rows = B * T * H
+    al = lambda x: (x + 255) // 256 * 256
+    want = 256 + al(B * T * 8) + al(ns * rows * 4) + al(ns * rows * 512 * 4)
+    assert va.workspace_bytes(B, T, H, ns) == want
+    assert lib.va_workspace_bytes(0, 16, 8, 1) == 0
+    assert lib.va_workspace_bytes(1, 65, 8, 1) == 0
+    assert lib.va_workspace_bytes(1, 16, 8, 0) == 0
+
+
+def _paged(lib, **over):
+    a = dict(q=A16, kv=A16, num_slots=4096, stride=576, slot=A16, indptr=A16, prefix=A16,
+             parent=A16, bits=None, B=1, T=4, H=8, scale=0.07, nsplit=4, flags=0, ws=A256,
+             ws_bytes=1 << 30, out=A16, lse=A16, stream=None)
+    a.update(over)
+    return lib.verify_attn_paged(a["q"], a["kv"], a["num_slots"], a["stride"], a["slot"],
+                                 a["indptr"], a["prefix"], a["parent"], a["bits"], a["B"], a["T"],
+                                 a["H"], a["scale"], a["nsplit"], a["flags"], a["ws"],
+                                 a["ws_bytes"], a["out"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(kv=None), -1), (dict(slot=None), -1), (dict(indptr=None), -1),
+    (dict(prefix=None), -1), (dict(ws=None), -1), (dict(out=None), -1), (dict(lse=None), -1),
+    (dict(parent=None, bits=None), -1),
+    (dict(B=0), -2), (dict(T=0), -2), (dict(T=65), -2), (dict(H=0), -2), (dict(num_slots=0), -2),
+    (dict(stride=512), -2), (dict(nsplit=-1), -2), (dict(nsplit=1025), -2), (dict(flags=7), -2),
+    (dict(scale=float("nan")), -2),
+    (dict(stride=580), -3), (dict(q=A16 + 8), -3), (dict(kv=A16 + 2), -3), (dict(out=A16 + 4), -3),
+    (dict(ws=A256 + 16), -3), (dict(lse=A16 + 2), -3), (dict(slot=A16 + 2), -3),
+    (dict(ws_bytes=1000), -4),
+])
+def test_paged_argument_errors(lib, over, code):
+    assert _paged(lib, **over) == code
+
+
+def test_valid_arguments_without_gpu_do_not_crash(lib):
+    # no device (or no va_init): an error code, never a crash
+    rc = _paged(lib)
+    assert rc in (-5, -7)
+
+
+def test_contiguous_argument_errors(lib):
+    f = lib.verify_attn_contiguous
+    base = [A16, A16, 4096, 576, A16, A16, A16, None, 1, 4, 8, 0.07, 4, 0, A256, 1 << 30, A16, A16,
+            None]
+    assert f(*base) in (-5, -7)
+    bad = list(base); bad[4] = None
+    assert f(*bad) == -1
+    bad = list(base); bad[4] = A16 + 4
+    assert f(*bad) == -3
+    bad = list(base); bad[15] = 10
+    assert f(*bad) == -4
+
+
+def test_defrag_argument_errors(lib):
+    f = lib.verify_attn_defrag
+    base = [A16, 4096, 576, A16, A16, A16, None, 1, 100, None, None]
+    assert f(*base) in (-5, -7)
+    for i, code in ((0, -1), (3, -1), (4, -1), (5, -1)):
+        bad = list(base); bad[i] = None
+        assert f(*bad) == code
+    bad = list(base); bad[7] = 0
+    assert f(*bad) == -2
+    bad = list(base); bad[2] = 584 + 4
+    assert f(*bad) == -3
+    bad = list(base); bad[0] = A16 + 8
+    assert f(*bad) == -3
+
+
+def test_read_status_null(lib):
+    assert lib.va_read_status(None, None, None) == -1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    monkeypatch.setattr(va, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(va, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        va.load()

@@ -1,0 +1,339 @@
+"""GPU vs fp64 oracle, element by element, through the C ABI (needs an sm_103 GPU).
+
+Bar: out max-abs <= 2e-2 and mean-abs <= 2e-3, lse abs <= 1e-3, on the same
+seeded inputs.  Integer results (defrag bytes, slot tables, status bits) are
+compared exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"fma": 1, "tc": 2}
+
+
+@pytest.fixture(scope="module")
+def va():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mla_speculative_decode_gb300 as m
+    m.build()
+    m.init()
+    return m
+
+
+def _need(va, path, B, T, H):
+    if path == PATHS["tc"]:
+        try:
+            va.auto_nsplit(B, T, H, path)
+        except va.VaError as e:
+            if e.code == -5:
+                pytest.skip("tensor-core path does not take this shape")
+            raise
+
+
+# ------------------------------------------------------------ small configs
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("name", ["tiny", "tp8"])
+def test_config_full_parity(va, name, path):
+    w = synth.make(synth.spec(name))
+    s = w.spec
+    _need(va, path, s.B, s.T, s.H)
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=path)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+SWEEP = [
+    # B, H, T, prefixes, tree, nsplit
+    (1, 1, 1, [0], "chain", 1),
+    (1, 1, 1, [1], "chain", 4),
+    (1, 8, 3, [63], "random", 2),
+    (1, 8, 5, [64], "random", 3),
+    (1, 8, 7, [65], "flat", 16),
+    (1, 16, 16, [127], "random", 64),
+    (1, 8, 16, [128], "random", 1),
+    (1, 8, 16, [129], "random", 128),
+    (1, 2, 64, [200], "random", 5),
+    (1, 4, 64, [1000], "chain", 7),
+    (3, 8, 9, [0, 300, 77], "random", 4),
+    (2, 16, 4, [513, 1], "random", 0),
+    (1, 64, 2, [2049], "random", 0),
+    (1, 5, 13, [777], "random", 0),
+]
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("B,H,T,prefix,tree,nsplit", SWEEP)
+def test_shape_sweep(va, B, H, T, prefix, tree, nsplit, path):
+    _need(va, path, B, T, H)
+    seed = hash((B, H, T, tuple(prefix))) % 1000
+    s = synth.Spec("sweep", B=B, H=H, T=T, prefix=prefix, num_slots=8192, tree=tree, seed=seed)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=path, nsplit=nsplit)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_canary_unreferenced_rows_are_nan(va, path):
+    """Every pool row and padding column the step must not read holds bf16 NaN:
+    a stray read poisons the output."""
+    for name in ("tiny", "tp8"):
+        s = synth.spec(name, canary=True, seed=synth.spec(name).seed + 100, row_stride=640,
+                       num_slots=1 << 16)
+        _need(va, path, s.B, s.T, s.H)
+        w = synth.make(s)
+        d = _gpu.to_device(w)
+        out, lse = _gpu.run(va, d, w, path=path)
+        ref_o, ref_l = _gpu.reference(w)
+        _gpu.compare(out, lse, ref_o, ref_l)
+
+
+# -------------------------------------------- full sizes, sampled rows
+
+@pytest.mark.parametrize("name", ["fullh", "long", "batched"])
+def test_full_size_sampled_rows(va, name):
+    """The large configurations at the benchmark's launch setting (automatic
+    split count), checked on sampled rows the oracle evaluates one by one."""
+    w = synth.make(synth.spec(name))
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=0)
+    rows = _gpu.sample_rows(w, 48, seed=1)
+    ref_o, ref_l = _gpu.reference(w, rows=rows)
+    _gpu.compare(out, lse, ref_o, ref_l, rows=rows)
+
+
+def test_long_nsplit_sweep(va):
+    """The long-context config at every split count of the sweep agrees with
+    the oracle and with itself (splits change rounding only)."""
+    w = synth.make(synth.spec("long"))
+    d = _gpu.to_device(w)
+    rows = _gpu.sample_rows(w, 24, seed=2)
+    ref_o, ref_l = _gpu.reference(w, rows=rows)
+    for ns in (16, 32, 64, 96, 128):
+        out, lse = _gpu.run(va, d, w, path=0, nsplit=ns)
+        _gpu.compare(out, lse, ref_o, ref_l, rows=rows)
+
+
+# -------------------------------------------------------- layout variants
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_contiguous_matches_oracle_and_paged(va, path):
+    s = synth.Spec("contig", B=3, H=8, T=16, prefix=[700, 64, 2000], num_slots=1 << 14,
+                   layout="contiguous", seed=31)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    out_c, lse_c = _gpu.run(va, d, w, path=path, layout="contiguous", nsplit=8)
+    out_p, lse_p = _gpu.run(va, d, w, path=path, layout="scattered", nsplit=8)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out_c, lse_c, ref_o, ref_l)
+    assert torch.equal(out_c, out_p) and torch.equal(lse_c, lse_p)
+
+
+def test_tree_bits_input_equals_parents(va):
+    w = synth.make(synth.spec("tp8"))
+    d = _gpu.to_device(w)
+    bits, _ = oracle.tree_bits(w.parents.numpy())
+    bits_t = torch.from_numpy(bits.view(np.int64)).cuda()
+    o1, l1 = _gpu.run(va, d, w, bits=bits_t)
+    o2, l2 = _gpu.run(va, d, w)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_paths_agree_with_each_other(va):
+    w = synth.make(synth.spec("tp8"))
+    s = w.spec
+    d = _gpu.to_device(w)
+    o1, l1 = _gpu.run(va, d, w, path=1)
+    try:
+        va.auto_nsplit(s.B, s.T, s.H, 2)
+    except va.VaError:
+        pytest.skip("tensor-core path does not take this shape")
+    o2, l2 = _gpu.run(va, d, w, path=2)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2 * _gpu.OUT_MAX_ABS
+    assert (l1 - l2).abs().max().item() <= 2 * _gpu.LSE_ABS
+
+
+# ------------------------------------------------ capture, determinism
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_graph_capture_replay_with_new_inputs(va, path):
+    """Capture one call, then change prefix lengths, slots, parents and q in
+    place: the replay equals a fresh eager call bit for bit."""
+    s = synth.Spec("cap", B=2, H=8, T=16, prefix=[3000, 1500], num_slots=1 << 15, seed=41)
+    _need(va, path, s.B, s.T, s.H)
+    w1 = synth.make(s)
+    w2 = synth.make(synth.Spec("cap", B=2, H=8, T=16, prefix=[2500, 2900], num_slots=1 << 15,
+                               seed=42))
+    w2.kv_pool = w1.kv_pool
+    d = _gpu.to_device(w1)
+    cap = max(w1.slot_idx.numel(), w2.slot_idx.numel())
+    slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    slots[:w1.slot_idx.numel()] = d["slot_idx"]
+    d["slot_idx"] = slots
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, 0, path)
+    out = torch.empty(s.B * s.T, s.H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(s.B * s.T, s.H, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        _gpu.run(va, d, w1, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _gpu.run(va, d, w1, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
+    g.replay()
+    torch.cuda.synchronize()
+    ref1_o, ref1_l = _gpu.reference(w1)
+    _gpu.compare(out, lse, ref1_o, ref1_l)
+    # new step: same buffers, new contents
+    d["q"].copy_(w2.q.cuda())
+    d["slot_idx"][:w2.slot_idx.numel()].copy_(w2.slot_idx.cuda())
+    d["kv_indptr"].copy_(w2.kv_indptr.cuda())
+    d["prefix_len"].copy_(w2.prefix_len.cuda())
+    d["parents"].copy_(w2.parents.cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    o_rep, l_rep = out.clone(), lse.clone()
+    o_eager, l_eager = _gpu.run(va, d, w2, path=path, nsplit=ns)
+    torch.cuda.synchronize()
+    assert torch.equal(o_rep, o_eager) and torch.equal(l_rep, l_eager)
+    ref2_o, ref2_l = _gpu.reference(w2)
+    _gpu.compare(o_rep, l_rep, ref2_o, ref2_l)
+    assert va.read_status(ws) == 0
+
+
+def test_deterministic(va):
+    w = synth.make(synth.spec("tp8"))
+    d = _gpu.to_device(w)
+    o1, l1 = _gpu.run(va, d, w, nsplit=37)
+    o2, l2 = _gpu.run(va, d, w, nsplit=37)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# -------------------------------------------------- guards and status
+
+def test_guard_regions_untouched(va):
+    w = synth.make(synth.spec("tiny"))
+    s = w.spec
+    d = _gpu.to_device(w)
+    ns = 6
+    n_ws = va.workspace_bytes(s.B, s.T, s.H, ns)
+    G = 4096
+    ws_big = torch.full((n_ws + 2 * G,), 0xA5, dtype=torch.uint8, device="cuda")
+    rows = s.B * s.T
+    out_big = torch.full((rows * s.H * 512 + 2 * G,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse_big = torch.full((rows * s.H + 2 * G,), 3.0, dtype=torch.float32, device="cuda")
+    ws = ws_big[G:G + n_ws]
+    out = out_big[G:G + rows * s.H * 512].view(rows, s.H, 512)
+    lse = lse_big[G:G + rows * s.H].view(rows, s.H)
+    _gpu.run(va, d, w, nsplit=ns, workspace=ws, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(ws_big[:G] == 0xA5) and torch.all(ws_big[G + n_ws:] == 0xA5)
+    assert torch.all(out_big[:G] == 7.0) and torch.all(out_big[G + rows * s.H * 512:] == 7.0)
+    assert torch.all(lse_big[:G] == 3.0) and torch.all(lse_big[G + rows * s.H:] == 3.0)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_bad_slot_is_skipped_and_flagged(va, path):
+    s = synth.Spec("bad", B=1, H=8, T=16, prefix=[300], num_slots=4096, seed=51)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    w.slot_idx[7] = 4096 + 3
+    w.slot_idx[150] = -5
+    d = _gpu.to_device(w)
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, 0, path)
+    out, lse = _gpu.run(va, d, w, path=path, nsplit=ns, workspace=ws)
+    assert va.read_status(ws) & va.STATUS_BAD_SLOT
+    ref_o, ref_l = _gpu.reference(w)      # the oracle skips the same keys
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+def test_bad_parent_flagged(va):
+    s = synth.Spec("badp", B=2, H=4, T=8, prefix=[100, 50], num_slots=4096, seed=52)
+    w = synth.make(s)
+    w.parents[1, 5] = 6       # not an earlier node
+    d = _gpu.to_device(w)
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, 0)
+    out, lse = _gpu.run(va, d, w, nsplit=ns, workspace=ws)
+    assert va.read_status(ws) == va.STATUS_BAD_PARENT
+    ref_o, ref_l = _gpu.reference(w)      # oracle: that node hangs off the prefix
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+def test_short_slot_list_flagged(va):
+    s = synth.Spec("short", B=2, H=4, T=8, prefix=[100, 50], num_slots=4096, seed=53)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    d["prefix_len"][1] = 80   # slot list of request 1 holds only 50 + 8 keys
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, 0)
+    out, lse = _gpu.run(va, d, w, nsplit=ns, workspace=ws)
+    assert va.read_status(ws) == va.STATUS_BAD_INDPTR
+    assert torch.isfinite(out.float()).all()
+    # request 0 is unaffected
+    ref_o, ref_l = _gpu.reference(w)
+    rows0 = s.T * s.H
+    _gpu.compare(out[:s.T], lse[:s.T], ref_o[:rows0], ref_l[:rows0])
+
+
+# ------------------------------------------------------------------ defrag
+
+def test_defrag_byte_exact_and_attention_preserved(va):
+    s = synth.Spec("defrag", B=3, H=8, T=16, prefix=[500, 1200, 64], num_slots=1 << 13, seed=61)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    # destinations: a fresh upper half of the pool that no live row uses
+    extra = synth._bf16_normal((s.num_slots, 576), torch.Generator().manual_seed(62))
+    w.kv_pool = torch.cat([w.kv_pool, extra])
+    d["kv_pool"] = w.kv_pool.cuda()
+    N = [p + s.T for p in s.prefix]
+    dst, pos = [], s.num_slots + 17
+    for n in N:
+        dst.append(pos)
+        pos += n + 5
+    dst_t = torch.tensor(dst, dtype=torch.int64)
+    out0, lse0 = _gpu.run(va, d, w, nsplit=4)
+    pool_ref, slots_ref = oracle.defrag(synth.as_u16(w.kv_pool), w.slot_idx.numpy(),
+                                        w.kv_indptr.numpy().astype(np.int64), dst_t.numpy())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    new_slots = d["slot_idx"].clone()
+    va.verify_attn_defrag(d["kv_pool"], d["slot_idx"], d["kv_indptr"], dst_t.cuda(),
+                          slot_idx_out=new_slots, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got_pool = d["kv_pool"].cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got_pool, pool_ref)
+    np.testing.assert_array_equal(new_slots.cpu().numpy(), slots_ref)
+    # paged over the new table and contiguous over dst_base both reproduce the step
+    d["slot_idx"] = new_slots
+    out1, lse1 = _gpu.run(va, d, w, nsplit=4, layout="scattered")
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    d["kv_start"] = dst_t.cuda()
+    out2, lse2 = _gpu.run(va, d, w, nsplit=4, layout="contiguous")
+    assert torch.equal(out0, out2) and torch.equal(lse0, lse2)
+
+
+def test_defrag_bad_rows_flagged_not_written(va):
+    pool = torch.randn(256, 576).to(torch.bfloat16).cuda()
+    before = pool.clone()
+    src = torch.tensor([3, 300, 5], dtype=torch.int32, device="cuda")
+    ip = torch.tensor([0, 3], dtype=torch.int32, device="cuda")
+    dst = torch.tensor([254], dtype=torch.int64, device="cuda")   # third row would land at 256
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    va.verify_attn_defrag(pool, src, ip, dst, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == va.STATUS_BAD_SLOT | va.STATUS_BAD_DST
+    assert torch.equal(pool[254], before[3])
+    assert torch.equal(pool[:254], before[:254]) and torch.equal(pool[255], before[255])
