@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) partial_fma_kernel(Params p) {
           a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
-      const int idx0 = 2 * int(__brev(unsigned(lane)) >> 27);
+      const int idx0 = 2 * lane;   // lane bit 4 picked the upper 32, bit 3 the upper 16, ...
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int idx = idx0 + e;
