@@ -190,6 +190,38 @@ int verify_attn_defrag(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
                        uint32_t *status, va_stream_t stream);
 
 /*
+ * Paged verify attention that allocates nothing and takes no workspace.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot call cudaMalloc: a plugin inside a serving engine whose allocator
+ * owns all device memory (the engine reserves nearly every byte for its KV
+ * pool and gives plugins no allocation hook), or a caller on a latency path
+ * where cudaMalloc / cudaFree would synchronise the device.
+ *
+ * Arguments are those of verify_attn_paged without workspace and
+ * workspace_bytes; the caller still provides every input and out / lse.  The
+ * scratch is a fixed device array of VA_NOALLOC_SCRATCH_BYTES inside the
+ * library, one per GPU that loads it, held until the process exits.
+ *  - Sizes: with nsplit = 0 the split count is lowered until the scratch
+ *    layout fits; an explicit nsplit whose layout does not fit, or sizes for
+ *    which even one split does not fit, return VA_ERR_WORKSPACE.
+ *  - First call on a device (after va_init on it) resolves the array's device
+ *    address with cudaGetSymbolAddress; make that first call before any stream
+ *    capture.  The first call is not thread-safe.
+ *  - Every call shares the one array and leaves its contents behind; the call
+ *    clears its status word itself.  Calls that overlap on the GPU (other
+ *    streams, other threads) race on the array and must be serialised by the
+ *    caller.  The status word sits in that array; it cannot be read with
+ *    va_read_status.
+ */
+#define VA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int verify_attn_paged_noalloc(const void *q, const void *kv_pool, int64_t num_slots,
+                              int64_t kv_row_stride, const int32_t *slot_idx,
+                              const int32_t *kv_indptr, const int32_t *prefix_len,
+                              const int32_t *tree_parent, const uint64_t *tree_bits, int B, int T,
+                              int H, float sm_scale, int nsplit, int flags, void *out, float *lse,
+                              va_stream_t stream);
+
+/*
  * Benchmark helper: while both handles are non-NULL, every verify call on this
  * process records cudaEvent_t `before` on its stream immediately before it
  * launches the split-K partial kernel and `after` immediately after, so the

@@ -77,6 +77,9 @@ def load() -> ctypes.CDLL:
     lib.verify_attn_contiguous.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
+    lib.verify_attn_paged_noalloc.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32,
+                                              i32, i32, P, P, P]
+    lib.verify_attn_paged_noalloc.restype = i32
     lib.va_set_partial_events.argtypes = [P, P]
     lib.va_set_partial_events.restype = i32
     lib.va_read_status.argtypes = [P, P, P]
@@ -263,3 +266,32 @@ def set_partial_events(before=None, after=None) -> None:
         if e.cuda_event == 0:
             e.record()          # the handle is created on first record
     load().va_set_partial_events(before.cuda_event, after.cuda_event)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def verify_attn_paged_noalloc(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor,
+                              kv_indptr: torch.Tensor, prefix_len: torch.Tensor,
+                              tree_parent: Optional[torch.Tensor] = None,
+                              tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                              nsplit: int = 0, flags: int = PATH_AUTO, out: torch.Tensor,
+                              lse: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """verify_attn_paged without a workspace: the library's fixed scratch array is
+    used instead, so nothing is allocated.  `out` and `lse` must be given."""
+    init(q.device.index)
+    for t, n, dt in ((q, "q", torch.bfloat16), (kv_pool, "kv_pool", torch.bfloat16),
+                     (slot_idx, "slot_idx", torch.int32), (kv_indptr, "kv_indptr", torch.int32),
+                     (prefix_len, "prefix_len", torch.int32), (out, "out", torch.bfloat16),
+                     (lse, "lse", torch.float32)):
+        _dev(t, n, dt)
+    B = prefix_len.shape[0]
+    T = q.shape[0] // B
+    H = q.shape[1]
+    par, bits = _tree_args(tree_parent, tree_bits)
+    rc = load().verify_attn_paged_noalloc(
+        _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
+        _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,
+        _ptr(out), _ptr(lse), _stream(stream))
+    _check("verify_attn_paged_noalloc", rc)
+    return out, lse

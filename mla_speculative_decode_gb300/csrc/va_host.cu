@@ -142,6 +142,13 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   return VA_OK;
 }
 
+// Scratch of verify_attn_paged_noalloc: one fixed device array per GPU that
+// loads this library, held until the process exits.  Host code must not pass
+// the symbol itself to a kernel (on the host it names a host-side stand-in);
+// it passes the device address from cudaGetSymbolAddress instead.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[VA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices];   // device address per device, set on first use
+
 }  // namespace
 
 VA_API int va_version(void) { return 100; }
@@ -224,6 +231,43 @@ VA_API int verify_attn_defrag(void* kv_pool, int64_t num_slots, int64_t kv_row_s
                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VA_ERR_LAUNCH;
   return VA_OK;
+}
+
+VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t num_slots,
+                                     int64_t kv_row_stride, const int32_t* slot_idx,
+                                     const int32_t* kv_indptr, const int32_t* prefix_len,
+                                     const int32_t* tree_parent, const uint64_t* tree_bits, int B,
+                                     int T, int H, float sm_scale, int nsplit, int flags,
+                                     void* out, float* lse, va_stream_t stream) {
+  if (B < 1 || T < 1 || T > VA_T_MAX || H < 1 || nsplit < 0 || nsplit > VA_NSPLIT_MAX)
+    return VA_ERR_SHAPE;
+  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC) return VA_ERR_SHAPE;
+  const size_t cap = VA_NOALLOC_SCRATCH_BYTES;
+  // an explicit split count that does not fit is rejected before any CUDA call
+  if (nsplit > 0 && va::ws_layout(B, T, H, nsplit).total > cap) return VA_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VA_ERR_CUDA;
+  DeviceState ds;
+  int rc = current_state(&ds);
+  if (rc != VA_OK) return rc;
+  if (!g_noalloc_ptr[dev]) {
+    // first call on this device: resolve the array's device address once
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return VA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  int ns = nsplit;
+  if (ns == 0) {
+    const int path = pick_path(flags, B, T, H);
+    if (path < 0) return VA_ERR_UNSUPPORTED;
+    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.num_sms)
+                            : auto_nsplit_fma(B, T, H, ds.num_sms);
+    while (ns > 1 && va::ws_layout(B, T, H, ns).total > cap) --ns;
+  }
+  if (va::ws_layout(B, T, H, ns).total > cap) return VA_ERR_WORKSPACE;
+  return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr,
+                       prefix_len, tree_parent, tree_bits, B, T, H, sm_scale, ns, flags,
+                       g_noalloc_ptr[dev], cap, out, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_API int va_set_partial_events(void* before, void* after) {
