@@ -54,18 +54,13 @@ static double widen_bf16(uint16_t h)
 int oracle_tree_bits(const int32_t *parent, int T, uint64_t *bits)
 {
     int bad = 0;
+    /* nodes are in topological order, so a node's set is its own bit plus
+       the (already built) set of its parent */
     for (int i = 0; i < T; ++i) {
         uint64_t set = 1ull << i;
         int p = parent[i];
-        if (p < -1 || p >= i) {
-            ++bad;
-        } else {
-            /* walk to the root one parent at a time */
-            while (p >= 0) {
-                set |= 1ull << p;
-                p = parent[p];
-            }
-        }
+        if (p < -1 || p >= i) ++bad;
+        else if (p >= 0) set |= bits[p];
         bits[i] = set;
     }
     return bad;

@@ -103,6 +103,16 @@ def test_tree_bits_bad_parent_counted(oracle_mod):
     assert int(bits[3]) == (1 << 3) | (1 << 1) | 1
 
 
+def test_tree_bits_child_of_bad_node(oracle_mod):
+    """A node whose parent is invalid hangs off the prefix; its children see
+    it and nothing above it (worked by hand)."""
+    parent = np.array([-1, 0, 7, 2, -1, 3], dtype=np.int32)   # node 2's parent is not earlier
+    bits, bad = oracle_mod.tree_bits(parent)
+    assert bad == 1
+    np.testing.assert_array_equal(bits, np.array([0b1, 0b11, 0b100, 0b1100, 0b10000, 0b101100],
+                                                 dtype=np.uint64))
+
+
 def test_extend_mask_golden_through_attention(oracle_mod):
     """q = 0 gives uniform weights over the visible keys; one-hot value rows then
     read the visible set straight out of the attention output."""
