@@ -7,7 +7,7 @@
 //     lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) o_s
 // with a max shift, splits at -inf skipped and a row with no key at all
 // producing out = 0, lse = -inf.  The split order is fixed, so the result is
-// deterministic.  A CTA of 128 threads merges one row, 4 columns per thread.
+// deterministic.
 //
 // Defragmentation (The Checkpoint Report, "Input Knowledge Required": keep
 // each request's KV contiguous).  A warp copies whole rows with 16-byte
@@ -19,46 +19,86 @@
 namespace va {
 namespace {
 
-constexpr int kCombineThreads = kDv / 4;
+constexpr int kCombineThreads = 256;   // 8 warps
+constexpr int kCombineCols = 128;      // value columns per CTA (a float4 per lane)
+constexpr int kMaxSplits = VA_NSPLIT_MAX;
 
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, w) : v + w;
+  }
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int i = 1; i < kCombineThreads / 32; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+  __syncthreads();
+  return r;
+}
+
+// Grid (row, 128-column chunk).  The split weights exp(lse_s - lse) are formed
+// once per CTA in shared memory; each warp then sums its share of the splits
+// for the chunk (a float4 per lane) and the eight partial sums are added.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
+  __shared__ float wsplit[kMaxSplits];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float4 part[kCombineThreads / 32][kCombineCols / 4];
   const int rows_total = p.B * p.rows_per_req;
-  const int tid = threadIdx.x;
-  for (int row = blockIdx.x; row < rows_total; row += gridDim.x) {
-    const int b = row / p.rows_per_req;
-    const ReqInfo ri = req_info(p, b, false);
-    const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
-    const float* pl = p.part_lse + row;
-    float m = -INFINITY;
-    for (int s = 0; s < ne; ++s) m = fmaxf(m, pl[size_t(s) * rows_total]);
-    float L = -INFINITY;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-      float z = 0.f;
-      for (int s = 0; s < ne; ++s) {
-        const float ls = pl[size_t(s) * rows_total];
-        if (ls != -INFINITY) z += expf(ls - m);
-      }
-      L = m + logf(z);
-      for (int s = 0; s < ne; ++s) {
-        const float ls = pl[size_t(s) * rows_total];
-        if (ls == -INFINITY) continue;
-        const float w = expf(ls - L);
-        const float4 o = *reinterpret_cast<const float4*>(
-            p.part_o + ((size_t)s * rows_total + row) * kDv + tid * 4);
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-      }
+  const int row = blockIdx.x, chunk = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = row / p.rows_per_req;
+  const ReqInfo ri = req_info(p, b, false);
+  const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
+  const float* pl = p.part_lse + row;
+
+  float m = -INFINITY;
+  for (int s = tid; s < ne; s += kCombineThreads) {
+    const float ls = pl[size_t(s) * rows_total];
+    wsplit[s] = ls;
+    m = fmaxf(m, ls);
+  }
+  m = block_reduce(m, red, true);
+  float z = 0.f;
+  if (m != -INFINITY)
+    for (int s = tid; s < ne; s += kCombineThreads)
+      if (wsplit[s] != -INFINITY) z += expf(wsplit[s] - m);
+  z = block_reduce(z, red, false);
+  const float L = m == -INFINITY ? -INFINITY : m + logf(z);
+  for (int s = tid; s < ne; s += kCombineThreads)
+    wsplit[s] = (L == -INFINITY || wsplit[s] == -INFINITY) ? 0.f : expf(wsplit[s] - L);
+  __syncthreads();
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
+  const size_t sstride = size_t(rows_total) * kDv;
+#pragma unroll 4
+  for (int s = warp; s < ne; s += kCombineThreads / 32) {
+    const float w = wsplit[s];
+    const float4 o = *reinterpret_cast<const float4*>(po + size_t(s) * sstride);
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) {
+      const float4 u = part[w][lane];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
     }
     uint2 packed;
-    packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-    packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + tid * 4) = packed;
-    if (tid == 0) p.lse[row] = L;
+    packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(t.x))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(t.y))) << 16);
+    packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(t.z))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(t.w))) << 16);
+    *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + chunk * kCombineCols + lane * 4) = packed;
+    if (chunk == 0 && lane == 0) p.lse[row] = L;
   }
 }
 
@@ -97,7 +137,7 @@ __global__ void __launch_bounds__(kDefragThreads)
 
 cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   const int rows_total = p.B * p.rows_per_req;
-  const int grid = rows_total < 65535 ? rows_total : 65535;
+  dim3 grid(unsigned(rows_total), unsigned(kDv / kCombineCols), 1u);
   combine_kernel<<<grid, kCombineThreads, 0, st>>>(p);
   return cudaGetLastError();
 }

@@ -145,6 +145,23 @@ __device__ inline uint32_t smem_u32(const void* ptr) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
 }
 
+// Event tracing for pipeline analysis.  Compiled out unless VA_TRACE is
+// defined; a traced build records %globaltimer per (role, event, tile) for the
+// first cluster of the grid into the device buffer `g_va_trace`, which the
+// translation unit that uses the macro defines.
+#ifdef VA_TRACE
+#define VA_TRACE_EVENT(role, ev, t)                                                        \
+  do {                                                                                   \
+    if (g_va_trace && blockIdx.x < 2 && blockIdx.y == 0 && blockIdx.z == 0 && (t) < 512) { \
+      unsigned long long _ts;                                                             \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                              \
+      g_va_trace[((role) * 8 + (ev)) * 512 + (t)] = _ts;                                  \
+    }                                                                                    \
+  } while (0)
+#else
+#define VA_TRACE_EVENT(role, ev, t) ((void)0)
+#endif
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_tree_bits(const Params& p, uint64_t* bits_out, cudaStream_t st);
 cudaError_t launch_partial_fma(const Params& p, int num_sms, cudaStream_t st);

@@ -7,10 +7,12 @@
 // call by clearing the workspace status word, so it runs even when the caller
 // supplies the masks itself.
 //
-// One CTA; a warp per request, one lane walking the nodes in order.  Since
-// parent[i] < i, node i's mask is its parent's mask plus its own bit.  A node
-// whose parent is not an earlier node is flagged and treated as a child of the
-// prefix.
+// One CTA; a warp per request.  The request's parents are staged in shared
+// memory and each lane builds its own node's set by walking up the tree
+// (indices strictly decrease, so at most T steps).  A node whose parent is
+// not an earlier node is flagged and treated as hanging off the prefix; the
+// walk stops there too, which is the same as taking node i's set as its own
+// bit plus its parent's set.
 #include "va_common.cuh"
 
 namespace va {
@@ -19,24 +21,31 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) tree_bits_kernel(Params p, uint64_t* bits_out) {
-  __shared__ uint64_t masks[kWarps][kTmax];
+  __shared__ int par[kWarps][kTmax];
   if (threadIdx.x == 0) *p.status = 0u;
   __syncthreads();
   if (p.tree_parent == nullptr) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int b = warp; b < p.B; b += kWarps) {
-    if (lane == 0) {
-      bool bad = false;
-      for (int i = 0; i < p.T; ++i) {
-        int par = p.tree_parent[size_t(b) * p.T + i];
-        uint64_t m = 1ull << i;
-        if (par < -1 || par >= i) bad = true;
-        else if (par >= 0) m |= masks[warp][par];
-        masks[warp][i] = m;
-        bits_out[size_t(b) * p.T + i] = m;
+    for (int i = lane; i < p.T; i += 32) par[warp][i] = p.tree_parent[size_t(b) * p.T + i];
+    __syncwarp();
+    bool bad = false;
+    for (int i = lane; i < p.T; i += 32) {
+      uint64_t m = 1ull << i;
+      int q = par[warp][i];
+      if (q < -1 || q >= i) {
+        bad = true;
+      } else {
+        while (q >= 0) {
+          m |= 1ull << q;
+          const int up = par[warp][q];
+          if (up < -1 || up >= q) break;
+          q = up;
+        }
       }
-      if (bad) atomicOr(p.status, VA_STATUS_BAD_PARENT);
+      bits_out[size_t(b) * p.T + i] = m;
     }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, VA_STATUS_BAD_PARENT);
     __syncwarp();
   }
 }

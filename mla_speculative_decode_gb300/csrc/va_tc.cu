@@ -1,11 +1,568 @@
-// va_tc.cu -- tcgen05 tensor-core split-K partial kernel (K1, TC path).
+// va_tc.cu -- split-K partial kernel on the tcgen05 tensor cores (K1, TC path).
+//
+// The step is two dense contractions over a shared latent row (The Milestone
+// Commit, "Input Knowledge Required": the draft tokens attend the full KV
+// cache; every head reads the same MLA latent row): S = Q K^T over 576
+// columns and O = P V over 512, with R = T*H rows per request.  On GB300 the
+// accumulator of one 128-row block, O = 128 x 512 fp32, fills a whole SM's
+// tensor memory (512 columns).  So each (split, 128-row block) runs on a
+// cluster of two CTAs on two SMs, with no duplicated work:
+//
+//   QK CTA (cluster rank 0)
+//     TMEM: Q as the A operand (128 lanes x 288 columns of bf16 pairs) and two
+//     64-column S buffers.  Warps 0, 2, 3 gather 64-key tiles with 16-byte
+//     cp.async copies written straight into the 128B-swizzled K-major layout
+//     into 3 stages of 72 KB; warp 1 issues S = Q K^T (36 MMAs of 128x64x16,
+//     A from TMEM, B K-major); warps 4-7 own a row each: read S, mask, online
+//     softmax with a conditional rescale (the reference max only moves when a
+//     tile exceeds it by 2^8), round P to bf16 and store it straight into the
+//     PV CTA's shared memory (distributed shared memory), with the row's
+//     rescale factor.
+//   PV CTA (cluster rank 1)
+//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3 gather the value
+//     columns (first 512) of the same tiles -- L2 hits behind the QK CTA's
+//     reads -- into 2 stages of 64 KB; warp 1 issues O += P V (8 MMAs of
+//     128x256x16, A = P K-major, B = V MN-major: the gathered tile is K-major
+//     for S and MN-major for PV); warps 4-7 rescale O rows on the rare tiles
+//     whose reference max moved, then normalise and write the split's partial.
+//
+// The design follows the pages' split-K / online-softmax / partial-reduce
+// structure (The Milestone Commit, "The Thinking Process Revealed"; The Commit
+// That Locked In 6x Decode, "Input Knowledge Required"), moved onto tcgen05,
+// TMEM and distributed shared memory.  Every wait is bounded: on timeout the
+// CTA sets VA_STATUS_TIMEOUT, stops, drains its own copies and MMAs, frees its
+// tensor memory and returns.
+#include <math.h>
+
 #include "va_common.cuh"
+#include "va_sm100.cuh"
+
+#ifdef VA_TRACE
+__device__ unsigned long long* g_va_trace = nullptr;
+extern "C" __attribute__((visibility("default"))) int va_trace_set(void* buf) {
+  return cudaMemcpyToSymbol(g_va_trace, &buf, sizeof(buf)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 namespace va {
+namespace {
 
-bool tc_supported(int, int, int) { return false; }
-int tc_auto_nsplit(int, int, int, int) { return 1; }
-cudaError_t init_partial_tc() { return cudaSuccess; }
-cudaError_t launch_partial_tc(const Params&, int, cudaStream_t) { return cudaErrorNotSupported; }
+using namespace sm100;
+
+constexpr int kThreads = 256;
+constexpr int kRows = 128;
+constexpr int kTile = 64;                                   // keys per tile
+constexpr int kKBlocks = kDqk / 64;                         // 9 column blocks (K)
+constexpr int kVBlocks = kDv / 64;                          // 8 column blocks (V)
+constexpr uint32_t kBlockBytes = kTile * 128;               // 8 KB: 64 keys x 64 cols
+constexpr uint32_t kKStageBytes = kKBlocks * kBlockBytes;   // 72 KB
+constexpr uint32_t kVStageBytes = kVBlocks * kBlockBytes;   // 64 KB
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr uint32_t kPBytes = kRows * 128;                   // P tile: 128 rows x 64 keys bf16
+
+// shared layout (offsets from a 1024-byte aligned base; identical in both CTAs
+// so that remote addresses and multicast commits land on the right objects)
+constexpr uint32_t kOffBars = 0;
+constexpr uint32_t kOffTmemSlot = 256;
+constexpr uint32_t kOffAbort = 260;
+constexpr uint32_t kOffCmd = 264;                           // PV: row-warp command word
+constexpr uint32_t kOffFlags = 512;                         // PV: uint32 [2][4] per-warp rescale flags
+constexpr uint32_t kOffValid = 576;                         // QK: uint64 [8] key-validity ring
+constexpr uint32_t kOffAlpha = 1024;                        // PV: float [2][128]
+constexpr uint32_t kOffFin = 2048;                          // PV: float [128]
+constexpr uint32_t kOffSrow = 2560;                         // int32 [3][64] staged pool rows
+constexpr uint32_t kOffK = 4096;                            // QK CTA: K stages
+constexpr uint32_t kOffP = 4096;                            // PV CTA: P buffers
+constexpr uint32_t kOffV = kOffP + 2 * kPBytes;             // PV CTA: V stages
+constexpr uint32_t kEndQK = kOffK + kKStages * kKStageBytes;
+constexpr uint32_t kEndPV = kOffV + kVStages * kVStageBytes;
+constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kValidRing = 8;
+constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
+
+enum : int {
+  B_KFULL = 0, B_KEMPTY = 3, B_SFULL = 6, B_SEMPTY = 8, B_PFREE = 10, B_QREADY = 12,
+  B_MMAFIN = 13, B_VFULL = 14, B_VEMPTY = 16, B_PFULL = 18, B_OGO = 20, B_OCORR = 21,
+  B_ODONE = 22, B_FIN = 23, kNumBars = 24
+};
+static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemQ = 0;      // QK CTA: Q, 288 columns
+constexpr uint32_t kTmemS = 320;    // QK CTA: S buffers at 320 and 384
+constexpr long long kWaitCycles = 4000000000ll;   // wait bound in SM cycles (~2 s)
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kProducers = 96;        // warps 0, 2, 3
+constexpr uint32_t kProducerBar = 1;  // named barrier of the producer warps
+
+// Two probabilities rounded to bf16 for the PV product; the row sum takes the
+// unrounded values so that lse stays exact to fp32 rounding.
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sum) {
+  sum += a + b;
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
+// Pool row of key j of the split, or -1 when j is past the split or has no
+// valid slot (its copy then zero-fills).
+__device__ __forceinline__ int key_row_or_none(const Params& p, const ReqInfo& ri, int j, int k1) {
+  if (j >= k1) return -1;
+  const int64_t r = key_row(p, ri, j);
+  return r >= 0 ? int(r) : -1;
+}
+
+// Producer warps (96 threads): gather each 64-key tile into the stage ring
+// with 16-byte cp.async copies written straight into the 128B-swizzled layout
+// (column block c/8, row `key`, 16-byte chunk (c%8) ^ (key%8)).  The tile's
+// pool rows are staged in shared memory and fetched one tile ahead; with
+// kMask the tile's 64-bit key-validity mask goes to the ring read by the
+// softmax warps.  Completion: every producer's cp.async arrival (noinc) plus,
+// with kMask, one plain arrival after the mask is written.  Returns false when
+// a bounded wait gave up (all producers agree through the named barrier).
+template <int kChunks, int kStages, bool kMask>
+__device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, const SplitRange& sr,
+                                        int ntiles, int ptid, uint32_t stage_base,
+                                        uint32_t stage_bytes, uint32_t full0, uint32_t empty0,
+                                        int* srow, uint32_t* valid32, volatile int* abort_flag) {
+  const int lane = ptid & 31;
+  int rw = ptid < 64 ? key_row_or_none(p, ri, sr.k0 + ptid, sr.k1) : -1;
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % kStages;
+    bool got = true;
+    if (t >= kStages)
+      got = mbar_wait(empty0 + 8u * uint32_t(s), uint32_t((t / kStages) - 1) & 1u, abort_flag,
+                      kWaitCycles);
+    if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
+    if (ptid < 64) {
+      srow[s * 64 + ptid] = rw;
+      if (kMask) {
+        const int j = sr.k0 + t * kTile + ptid;
+        if (j < sr.k1 && rw < 0) atomicOr(p.status, VA_STATUS_BAD_SLOT);
+        const uint32_t bal = __ballot_sync(0xffffffffu, rw >= 0);
+        if (lane == 0) valid32[(t % kValidRing) * 2 + (ptid >> 5)] = bal;
+      }
+    }
+    if (!named_sync_and(kProducerBar, kProducers, got)) {
+      ok = false;
+      break;
+    }
+    if (kMask && ptid == 0) mbar_arrive(full0 + 8u * uint32_t(s));
+    if (ptid < 64 && t + 1 < ntiles) rw = key_row_or_none(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
+    const uint32_t dst0 = stage_base + uint32_t(s) * stage_bytes;
+#pragma unroll 4
+    for (int idx = ptid; idx < 64 * kChunks; idx += kProducers) {
+      const int key = idx / kChunks, c = idx - key * kChunks;
+      const int row = srow[s * 64 + key];
+      const __nv_bfloat16* src = row >= 0 ? p.kv + int64_t(row) * p.kv_stride + c * 8 : p.kv;
+      const uint32_t dst = dst0 + uint32_t(c >> 3) * kBlockBytes + uint32_t(key) * 128u +
+                           uint32_t(((c & 7) ^ (key & 7)) * 16);
+      cp_async16(dst, src, row >= 0 ? 16u : 0u);
+    }
+    cp_async_arrive_noinc(full0 + 8u * uint32_t(s));
+    if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
+  }
+  cp_async_wait_all();
+  return ok;
+}
+
+// Q rows into TMEM as the A operand (bf16 pairs, 288 columns): each softmax
+// thread writes its own row (lane quadrant = warp % 4), 3 column chunks of
+// 32 (64 features each) per round trip to memory.
+__device__ __forceinline__ void load_q(const Params& p, int b, int row0, int warp, int lane,
+                                       uint32_t tmem) {
+  const int q4 = warp & 3;
+  const int lr = row0 + q4 * 32 + lane;
+  const bool ok = lr < p.rows_per_req;
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t(b) * p.rows_per_req + lr) * kDqk);
+  const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + kTmemQ;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kKBlocks; c0 += 3) {
+    uint4 buf[24];
+#pragma unroll
+    for (int i = 0; i < 24; ++i) buf[i] = ok ? src[c0 * 8 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int cc = 0; cc < 3; ++cc) {
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[4 * i] = buf[cc * 8 + i].x; v[4 * i + 1] = buf[cc * 8 + i].y;
+        v[4 * i + 2] = buf[cc * 8 + i].z; v[4 * i + 3] = buf[cc * 8 + i].w;
+      }
+      tmem_st32(tl + 32u * uint32_t(c0 + cc), v);
+    }
+  }
+  tmem_wait_st();
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    partial_tc_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (sb - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kOffAbort);
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBars + 8u * uint32_t(i); };
+
+  const uint32_t rank = cluster_ctarank();
+  const int split = blockIdx.x >> 1, rb = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const ReqInfo ri = req_info(p, b, split == 0 && rb == 0 && rank == 0 && tid == 0);
+  const SplitRange sr = split_range(ri.N, p.nsplit, split);
+  if (split >= sr.nsplit_eff) return;   // both CTAs of the cluster leave together
+  const int R = p.rows_per_req;
+  const int row0 = rb * kRows;
+  const int ntiles = ceil_div(sr.k1 - sr.k0, kTile);
+  const size_t rows_total = size_t(p.B) * R;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(p.status, VA_STATUS_TIMEOUT);
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_OCORR || i == B_QREADY) cnt = 128;
+      if (i >= B_KFULL && i < B_KFULL + kKStages) cnt = kProducers + 1;   // copies + mask
+      if (i >= B_VFULL && i < B_VFULL + kVStages) cnt = kProducers;
+      if (i == B_PFULL || i == B_PFULL + 1 || i == B_FIN) cnt = 4;   // one per softmax warp
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tmem_alloc(sb + kOffTmemSlot, kTmemCols);
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
+  const bool producer = warp == 0 || warp == 2 || warp == 3;
+  const int ptid = warp == 0 ? lane : (warp - 1) * 32 + lane;
+  int* srow = reinterpret_cast<int*>(gb + kOffSrow);
+
+  if (rank == 0) {
+    // ================================================================ QK CTA
+    volatile uint64_t* valid_ring = reinterpret_cast<volatile uint64_t*>(gb + kOffValid);
+    if (producer) {
+      // ---- producers: K tiles (all 576 columns)
+      if (!produce<kDqk / 8, kKStages, true>(p, ri, sr, ntiles, ptid, sb + kOffK, kKStageBytes,
+                                             bar(B_KFULL), bar(B_KEMPTY), srow,
+                                             reinterpret_cast<uint32_t*>(gb + kOffValid),
+                                             abort_flag) &&
+          ptid == 0)
+        fail();
+    } else if (warp == 1) {
+      // ---- MMA issuer: S[t%2] = Q K_t^T
+      if (lane == 0) {
+        bool ok = mbar_wait(bar(B_QREADY), 0, abort_flag, kWaitCycles);
+        if (!ok) fail();
+        constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+        for (int t = 0; ok && t < ntiles; ++t) {
+          const int s = t % kKStages, bs = t & 1;
+          if (!mbar_wait(bar(B_KFULL + s), uint32_t(t / kKStages) & 1u, abort_flag, kWaitCycles) ||
+              (t >= 2 && !mbar_wait(bar(B_SEMPTY + bs), uint32_t((t >> 1) - 1) & 1u, abort_flag,
+                                    kWaitCycles))) {
+            fail();
+            break;
+          }
+          fence_proxy_async_cta();   // the producers' cp.async writes, seen by the tensor core
+          tc_fence_after();
+          VA_TRACE_EVENT(1, 0, t);
+          const uint32_t kbase = sb + kOffK + uint32_t(s) * kKStageBytes;
+          const uint32_t d = tmem + kTmemS + 64u * uint32_t(bs);
+#pragma unroll 4
+          for (int k = 0; k < kDqk / 16; ++k) {
+            const uint64_t bd =
+                smem_desc(kbase + uint32_t(k >> 2) * kBlockBytes + uint32_t(k & 3) * 32u, 16, 1024,
+                          kSwizzle128B);
+            mma_ts(d, tmem + kTmemQ + 8u * uint32_t(k), bd, idesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(B_SFULL + bs));
+          mma_commit(bar(B_KEMPTY + s));
+          VA_TRACE_EVENT(1, 1, t);
+        }
+        mma_commit(bar(B_MMAFIN));
+        mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      // ---- softmax rows
+      load_q(p, b, row0, warp, lane, tmem);
+      tc_fence_before();
+      mbar_arrive(bar(B_QREADY));
+      const int q4 = warp & 3;
+      const int r = q4 * 32 + lane;
+      const int lr = row0 + r;
+      const bool row_ok = lr < R;
+      const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);
+      const uint64_t nbits = row_ok ? p.bits[size_t(b) * p.T + lr / p.H] : 0ull;
+      const uint32_t pv_p = mapa(sb + kOffP, 1);
+      const uint32_t pv_alpha = mapa(sb + kOffAlpha, 1);
+      const uint32_t pv_flags = mapa(sb + kOffFlags, 1);
+      const uint32_t pv_fin = mapa(sb + kOffFin, 1);
+      const uint32_t pv_pfull = mapa(bar(B_PFULL), 1);
+      const uint32_t pv_finbar = mapa(bar(B_FIN), 1);
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int t = 0; t < ntiles; ++t) {
+        const int bs = t & 1;
+        const int tk0 = sr.k0 + t * kTile;
+        // visibility: prefix keys always, draft key k when bit k of the node's mask
+        const int off = ri.P - tk0;
+        uint64_t vis;
+        if (off >= 64) {
+          vis = ~0ull;
+        } else if (off > 0) {
+          vis = ((1ull << off) - 1ull) | (nbits << off);
+        } else {
+          vis = (-off) >= 64 ? 0ull : (nbits >> (-off));
+        }
+        if (!row_ok) vis = 0ull;
+
+        // S_t ready (and, through the stage's full barrier, the producers'
+        // validity mask of this tile)
+        const bool got =
+            mbar_wait(bar(B_SFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
+            mbar_wait(bar(B_KFULL + t % kKStages), uint32_t(t / kKStages) & 1u, abort_flag,
+                      kWaitCycles);
+        if (!__all_sync(0xffffffffu, got)) {
+          fail();
+          ok = false;
+          break;
+        }
+        vis &= valid_ring[t % kValidRing];
+        if (tid == 128) VA_TRACE_EVENT(2, 0, t);
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tl + kTmemS + 64u * uint32_t(bs), s0);
+        tmem_ld32(tl + kTmemS + 64u * uint32_t(bs) + 32u, s1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(B_SEMPTY + bs));
+
+        float x[64];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = ((vis >> c) & 1ull) ? __uint_as_float(s0[c]) * p.scale_log2 : -INFINITY;
+          x[c + 32] = ((vis >> (c + 32)) & 1ull) ? __uint_as_float(s1[c]) * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, fmaxf(x[c], x[c + 32]));
+        }
+        float alpha = 1.f;
+        if (mt > m_ref + kRescaleLog2) {
+          alpha = ex2_approx(m_ref - mt);   // 0 when nothing was seen before
+          l *= alpha;
+          m_ref = mt;
+        }
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          pk[c] = pack_bf16(ex2_approx(x[2 * c] - mr), ex2_approx(x[2 * c + 1] - mr), l);
+        const uint32_t wres = __ballot_sync(0xffffffffu, alpha != 1.f);
+        if (tid == 128) VA_TRACE_EVENT(2, 1, t);
+
+        const bool freed = t < 2 || mbar_wait<true>(bar(B_PFREE + bs), uint32_t((t >> 1) - 1) & 1u,
+                                                    abort_flag, kWaitCycles);
+        if (!__all_sync(0xffffffffu, freed)) {
+          fail();
+          ok = false;
+          break;
+        }
+        if (tid == 128) VA_TRACE_EVENT(2, 2, t);
+        const uint32_t prow = pv_p + uint32_t(bs) * kPBytes + uint32_t(r) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_cluster_v4(prow + uint32_t((j ^ (r & 7)) * 16), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                        pk[4 * j + 3]);
+        st_cluster_f32(pv_alpha + uint32_t(bs * 128 + r) * 4u, alpha);
+        if (lane == 0)
+          st_cluster_u32(pv_flags + uint32_t(bs * 4 + q4) * 4u, (uint32_t(t) << 1) | (wres ? 1u : 0u));
+        fence_proxy_async_cluster();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(pv_pfull + 8u * uint32_t(bs));
+        if (tid == 128) VA_TRACE_EVENT(2, 3, t);
+      }
+      if (ok) {
+        const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        if (row_ok) p.part_lse[size_t(split) * rows_total + size_t(b) * R + lr] = lse;
+        st_cluster_f32(pv_fin + uint32_t(r) * 4u, l > 0.f ? 1.f / l : 0.f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(pv_finbar);
+        // the PV CTA's last releases of our P buffers have landed before we leave
+        for (int t = ntiles - 2 > 0 ? ntiles - 2 : 0; t < ntiles; ++t)
+          if (!mbar_wait<true>(bar(B_PFREE + (t & 1)), uint32_t(t >> 1) & 1u, abort_flag,
+                               kWaitCycles))
+            fail();
+      }
+    }
+  } else {
+    // ================================================================ PV CTA
+    volatile uint32_t* cmd = reinterpret_cast<volatile uint32_t*>(gb + kOffCmd);
+    if (producer) {
+      // ---- producers: value columns of the same tiles
+      if (!produce<kDv / 8, kVStages, false>(p, ri, sr, ntiles, ptid, sb + kOffV, kVStageBytes,
+                                             bar(B_VFULL), bar(B_VEMPTY), srow, nullptr,
+                                             abort_flag) &&
+          ptid == 0)
+        fail();
+    } else if (warp == 1) {
+      // ---- MMA issuer: O += P_t V_t
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(128, 256, 0, 1);
+        const volatile uint32_t* flags = reinterpret_cast<const volatile uint32_t*>(gb + kOffFlags);
+        uint32_t nresc = 0;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+          const int s = t % kVStages, bs = t & 1;
+          if (!mbar_wait(bar(B_VFULL + s), uint32_t(t / kVStages) & 1u, abort_flag, kWaitCycles) ||
+              !mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles)) {
+            fail();
+            ok = false;
+            break;
+          }
+          VA_TRACE_EVENT(4, 0, t);
+          uint32_t any = 0;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) any |= flags[bs * 4 + w] & 1u;
+          if (any && t > 0) {
+            // rows change reference: O must be final for tile t-1 before the
+            // row warps rescale it, and rescaled before this tile's product
+            mma_commit(bar(B_ODONE));
+            ok = mbar_wait(bar(B_ODONE), nresc & 1u, abort_flag, kWaitCycles);
+            if (ok) {
+              *cmd = uint32_t(bs);
+              mbar_arrive(bar(B_OGO));
+              ok = mbar_wait(bar(B_OCORR), nresc & 1u, abort_flag, kWaitCycles);
+            }
+            ++nresc;
+            if (!ok) {
+              fail();
+              break;
+            }
+          }
+          fence_proxy_async_cta();
+          tc_fence_after();
+          const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBytes;
+          const uint32_t vbase = sb + kOffV + uint32_t(s) * kVStageBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint64_t ad = smem_desc(pbase + uint32_t(k) * 32u, 16, 1024, kSwizzle128B);
+              const uint64_t bd = smem_desc(vbase + uint32_t(4 * h) * kBlockBytes + uint32_t(k) * 2048u,
+                                            kBlockBytes, 1024, kSwizzle128B);
+              mma_ss(tmem + 256u * uint32_t(h), ad, bd, idesc, (t > 0 || k > 0) ? 1u : 0u);
+            }
+          mma_commit(bar(B_VEMPTY + s));
+          mma_commit_mc(bar(B_PFREE + bs), uint16_t(1u << 0));
+          VA_TRACE_EVENT(4, 1, t);
+        }
+        // last command to the row warps: no more rescales
+        *cmd = kCmdDone;
+        mbar_arrive(bar(B_OGO));
+        mma_commit(bar(B_MMAFIN));
+        mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
+        (void)ok;
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      // ---- row warps: rescale O rows on command, then the split's partial
+      const int q4 = warp & 3;
+      const int r = q4 * 32 + lane;
+      const int lr = row0 + r;
+      const bool row_ok = lr < R;
+      const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);
+      const float* alpha_s = reinterpret_cast<const float*>(gb + kOffAlpha);
+      bool ok = true;
+      for (uint32_t k = 0;; ++k) {
+        const bool go = mbar_wait(bar(B_OGO), k & 1u, abort_flag, kWaitCycles);
+        if (!__all_sync(0xffffffffu, go)) {
+          fail();
+          ok = false;
+          break;
+        }
+        const uint32_t c = *cmd;
+        if (c == kCmdDone) break;
+        const float a = alpha_s[c * 128 + r];
+        tc_fence_after();
+        // tcgen05.ld/st are warp-collective: the whole warp takes part when
+        // any of its rows rescales, each lane scaling by its own factor
+        if (__any_sync(0xffffffffu, a != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 16; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tl + 32u * uint32_t(cc), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+            tmem_st32(tl + 32u * uint32_t(cc), v);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_OCORR));
+      }
+      const bool fin = ok && mbar_wait<true>(bar(B_FIN), 0, abort_flag, kWaitCycles) &&
+                       mbar_wait(bar(B_MMAFIN), 0, abort_flag, kWaitCycles);
+      if (__all_sync(0xffffffffu, fin)) {
+        tc_fence_after();
+        const float inv = reinterpret_cast<const float*>(gb + kOffFin)[r];
+        float* dst = p.part_o + (size_t(split) * rows_total + size_t(b) * R + lr) * kDv;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + 32u * uint32_t(c), v);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + 32 * c + e) =
+                  make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
+                              __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+          }
+        }
+      } else if (ok) {
+        fail();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  cluster_sync();
+}
+
+}  // namespace
+
+bool tc_supported(int, int, int) { return true; }
+
+int tc_auto_nsplit(int B, int T, int H, int num_sms) {
+  const long rowblocks = (long(T) * H + kRows - 1) / kRows;
+  const long items = rowblocks * B;
+  const long pairs = num_sms / 2;
+  long ns = pairs / items;
+  if (ns < 1) ns = 1;
+  if (ns > VA_NSPLIT_MAX) ns = VA_NSPLIT_MAX;
+  return int(ns);
+}
+
+cudaError_t init_partial_tc() {
+  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(kSmemBytes));
+}
+
+cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
+  dim3 grid(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
 
 }  // namespace va

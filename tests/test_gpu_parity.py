@@ -98,6 +98,26 @@ def test_canary_unreferenced_rows_are_nan(va, path):
         _gpu.compare(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_forced_rescales(va, path, nsplit):
+    """Later tiles whose scores jump far above the running maximum (the rotary
+    columns of their keys are scaled by 16 and 64; values are unchanged), so
+    the online softmax must move its reference and rescale the accumulator."""
+    s = synth.Spec("resc", B=1, H=8, T=16, prefix=[700], num_slots=4096, seed=81)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    for (j0, j1), f in (((192, 256), 16.0), ((448, 512), 64.0)):
+        rows = w.slot_idx[j0:j1].long()
+        w.kv_pool[rows, 512:576] *= f
+    d = _gpu.to_device(w)
+    ws, _ = va.alloc_workspace(s.B, s.T, s.H, nsplit, path)
+    out, lse = _gpu.run(va, d, w, path=path, nsplit=nsplit, workspace=ws)
+    assert va.read_status(ws) == 0
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
 # -------------------------------------------- full sizes, sampled rows
 
 @pytest.mark.parametrize("name", ["fullh", "long", "batched"])
