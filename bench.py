@@ -144,7 +144,7 @@ class Step:
     (disjoint random subsets of the pool) so that consecutive steps read rows
     that are not in L2."""
 
-    def __init__(self, va, pool, H, T, P, seed, nrot, dev, path, nsplit):
+    def __init__(self, va, pool, H, T, P, seed, nrot, dev, path, nsplit, layout="scattered"):
         self.va = va
         self.pool = pool
         self.H, self.T, self.P = H, T, P
@@ -156,7 +156,11 @@ class Step:
         if nrot * self.N > pool.shape[0]:
             nrot = max(1, pool.shape[0] // self.N)
         self.nrot = nrot
+        self.layout = layout
         self.tables = [perm[k * self.N:(k + 1) * self.N].to(torch.int32).to(dev)
+                       for k in range(nrot)]
+        # contiguous layout: rotation k reads pool rows [k*N, (k+1)*N)
+        self.starts = [torch.tensor([k * self.N], dtype=torch.int64, device=dev)
                        for k in range(nrot)]
         self.indptr = torch.tensor([0, self.N], dtype=torch.int32, device=dev)
         self.prefix = torch.tensor([P], dtype=torch.int32, device=dev)
@@ -167,6 +171,12 @@ class Step:
         self.kv_bytes = self.N * synth.D_QK * 2
 
     def call(self, k, stream=None):
+        if self.layout == "contiguous":
+            self.va.verify_attn_contiguous(self.q, self.pool, self.starts[k % self.nrot],
+                                           self.prefix, self.parents, sm_scale=synth.SM_SCALE,
+                                           nsplit=self.nsplit, flags=self.path, workspace=self.ws,
+                                           out=self.out, lse=self.lse, stream=stream)
+            return
         self.va.verify_attn_paged(self.q, self.pool, self.tables[k % self.nrot], self.indptr,
                                   self.prefix, self.parents, sm_scale=synth.SM_SCALE,
                                   nsplit=self.nsplit, flags=self.path, workspace=self.ws,
@@ -408,18 +418,20 @@ def main():
     # ---- prefix sweeps (H=8 and H=64, T=16), scattered slots
     sweep = []
     if not args.no_sweep and rank == 0:
-        for Hs in (8, 64):
-            for Ps in SWEEP_P:
+        points = [(Hs, Ps, "scattered") for Hs in (8, 64) for Ps in SWEEP_P]
+        points += [(Hs, Ps, "contiguous") for Hs in (8, 64) for Ps in (16384, 65536, 200000)]
+        for Hs, Ps, lay in points:
+            if True:
                 kvb = (Ps + 16) * synth.D_QK * 2
                 nr = max(1, min(16, math.ceil(3 * l2 / kvb)))
                 st = Step(va, pool, Hs, 16, Ps, seed=7, nrot=nr, dev=dev, path=args.path,
-                          nsplit=0)
+                          nsplit=0, layout=lay)
                 gs, ev = capture_graphs(st, with_events=True)
                 reps = max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8))))
                 tms = time_graphs(gs, reps, 5)
                 kms = kernel_ms(ev, reps)
                 us = tms / reps * 1e3
-                sweep.append({"H": Hs, "T": 16, "P": Ps, "us_per_step": us,
+                sweep.append({"H": Hs, "T": 16, "P": Ps, "layout": lay, "us_per_step": us,
                               "gbs": kvb / (us * 1e-6) / 1e9,
                               "frac_hbm": kvb / (us * 1e-6) / 1e9 / hbm_peak,
                               "partial_kernel_us": kms * 1e3,

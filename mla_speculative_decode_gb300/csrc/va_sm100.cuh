@@ -168,6 +168,19 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// --------------------------------------------------------------------- TMA
+
+// Tiled 2-D box load of a tensor map (`map` is a __grid_constant__ kernel
+// parameter); completes on `bar` with complete_tx.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int col, int row,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(col), "r"(row), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocates `ncols` TMEM columns (power of two >= 32); the address is written

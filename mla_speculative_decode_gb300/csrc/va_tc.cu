@@ -32,7 +32,10 @@
 // TMEM and distributed shared memory.  Every wait is bounded: on timeout the
 // CTA sets VA_STATUS_TIMEOUT, stops, drains its own copies and MMAs, frees its
 // tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+#include <string.h>
 
 #include "va_common.cuh"
 #include "va_sm100.cuh"
@@ -79,13 +82,16 @@ constexpr uint32_t kEndQK = kOffK + kKStages * kKStageBytes;
 constexpr uint32_t kEndPV = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Key-validity masks travel through their own ring of 8 barriers: the
+// producers run at most kKStages + 2 tiles ahead of the softmax warps, so a
+// parity wait on this ring is never two phases behind.
 constexpr int kValidRing = 8;
 constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
 
 enum : int {
   B_KFULL = 0, B_KEMPTY = 3, B_SFULL = 6, B_SEMPTY = 8, B_PFREE = 10, B_QREADY = 12,
   B_MMAFIN = 13, B_VFULL = 14, B_VEMPTY = 16, B_PFULL = 18, B_OGO = 20, B_OCORR = 21,
-  B_ODONE = 22, B_FIN = 23, kNumBars = 24
+  B_ODONE = 22, B_FIN = 23, B_VREADY = 24, kNumBars = 32
 };
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
 
@@ -113,19 +119,25 @@ __device__ __forceinline__ int key_row_or_none(const Params& p, const ReqInfo& r
   return r >= 0 ? int(r) : -1;
 }
 
-// Producer warps (96 threads): gather each 64-key tile into the stage ring
-// with 16-byte cp.async copies written straight into the 128B-swizzled layout
-// (column block c/8, row `key`, 16-byte chunk (c%8) ^ (key%8)).  The tile's
-// pool rows are staged in shared memory and fetched one tile ahead; with
-// kMask the tile's 64-bit key-validity mask goes to the ring read by the
-// softmax warps.  Completion: every producer's cp.async arrival (noinc) plus,
-// with kMask, one plain arrival after the mask is written.  Returns false when
-// a bounded wait gave up (all producers agree through the named barrier).
+// Producer warps (96 threads): bring each 64-key tile into the stage ring in
+// the 128B-swizzled K-major layout (column block c/8, row `key`, 16-byte
+// chunk (c%8) ^ (key%8)).
+//  - Paged keys, or a split's ragged last tile: 16-byte cp.async copies from
+//    every producer thread (zero-filled for keys without a row).  The tile's
+//    pool rows are staged in shared memory and fetched one tile ahead.
+//  - Contiguous keys (kv_start) for a whole in-range tile: one TMA tiled box
+//    load of 64 rows x 64 columns per column block.
+// With kMask the tile's 64-bit key-validity mask goes to the ring read by the
+// softmax warps.  Completion: every producer's cp.async arrival (noinc) plus
+// one arrival of producer 0 (with the TMA byte count when boxes are used,
+// after the mask is written).  Returns false when a bounded wait gave up (all
+// producers agree through the named barrier).
 template <int kChunks, int kStages, bool kMask>
 __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, const SplitRange& sr,
                                         int ntiles, int ptid, uint32_t stage_base,
                                         uint32_t stage_bytes, uint32_t full0, uint32_t empty0,
-                                        int* srow, uint32_t* valid32, volatile int* abort_flag) {
+                                        int* srow, uint32_t* valid32, uint32_t vready0,
+                                        volatile int* abort_flag, const CUtensorMap* tmap) {
   const int lane = ptid & 31;
   int rw = ptid < 64 ? key_row_or_none(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
@@ -149,11 +161,27 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
       ok = false;
       break;
     }
-    if (kMask && ptid == 0) mbar_arrive(full0 + 8u * uint32_t(s));
-    if (ptid < 64 && t + 1 < ntiles) rw = key_row_or_none(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
     const uint32_t dst0 = stage_base + uint32_t(s) * stage_bytes;
+    // contiguous rows, whole tile inside the split and the pool: box loads
+    const int tk0 = sr.k0 + t * kTile;
+    const int64_t row0 = p.kv_start ? ri.base + tk0 : -1;
+    const bool boxes = p.kv_start != nullptr && tk0 + kTile <= sr.k1 && tk0 + kTile <= ri.nlist &&
+                       row0 >= 0 && row0 + kTile <= p.num_slots && row0 + kTile <= 0x7fffffff;
+    if (kMask && ptid == 0) mbar_arrive(vready0 + 8u * uint32_t(t % kValidRing));
+    if (ptid == 0) {
+      if (boxes) {
+        mbar_arrive_expect_tx(full0 + 8u * uint32_t(s), uint32_t(kChunks / 8) * kBlockBytes);
+#pragma unroll 1
+        for (int c = 0; c < kChunks / 8; ++c)
+          tma_load_2d(dst0 + uint32_t(c) * kBlockBytes, tmap, 64 * c, int(row0),
+                      full0 + 8u * uint32_t(s));
+      } else {
+        mbar_arrive(full0 + 8u * uint32_t(s));
+      }
+    }
+    if (ptid < 64 && t + 1 < ntiles) rw = key_row_or_none(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
 #pragma unroll 4
-    for (int idx = ptid; idx < 64 * kChunks; idx += kProducers) {
+    for (int idx = ptid; !boxes && idx < 64 * kChunks; idx += kProducers) {
       const int key = idx / kChunks, c = idx - key * kChunks;
       const int row = srow[s * 64 + key];
       const __nv_bfloat16* src = row >= 0 ? p.kv + int64_t(row) * p.kv_stride + c * 8 : p.kv;
@@ -198,7 +226,7 @@ __device__ __forceinline__ void load_q(const Params& p, int b, int row0, int war
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    partial_tc_kernel(const __grid_constant__ Params p) {
+    partial_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -227,8 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_OCORR || i == B_QREADY) cnt = 128;
-      if (i >= B_KFULL && i < B_KFULL + kKStages) cnt = kProducers + 1;   // copies + mask
-      if (i >= B_VFULL && i < B_VFULL + kVStages) cnt = kProducers;
+      if (i >= B_KFULL && i < B_KFULL + kKStages) cnt = kProducers + 1;   // copies + producer 0
+      if (i >= B_VFULL && i < B_VFULL + kVStages) cnt = kProducers + 1;
       if (i == B_PFULL || i == B_PFULL + 1 || i == B_FIN) cnt = 4;   // one per softmax warp
       mbar_init(bar(i), cnt);
     }
@@ -251,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!produce<kDqk / 8, kKStages, true>(p, ri, sr, ntiles, ptid, sb + kOffK, kKStageBytes,
                                              bar(B_KFULL), bar(B_KEMPTY), srow,
                                              reinterpret_cast<uint32_t*>(gb + kOffValid),
-                                             abort_flag) &&
+                                             bar(B_VREADY), abort_flag, &tmap) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
@@ -322,11 +350,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!row_ok) vis = 0ull;
 
-        // S_t ready (and, through the stage's full barrier, the producers'
-        // validity mask of this tile)
+        // S_t ready, and the producers' validity mask of this tile
         const bool got =
             mbar_wait(bar(B_SFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
-            mbar_wait(bar(B_KFULL + t % kKStages), uint32_t(t / kKStages) & 1u, abort_flag,
+            mbar_wait(bar(B_VREADY + t % kValidRing), uint32_t(t / kValidRing) & 1u, abort_flag,
                       kWaitCycles);
         if (!__all_sync(0xffffffffu, got)) {
           fail();
@@ -405,8 +432,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (producer) {
       // ---- producers: value columns of the same tiles
       if (!produce<kDv / 8, kVStages, false>(p, ri, sr, ntiles, ptid, sb + kOffV, kVStageBytes,
-                                             bar(B_VFULL), bar(B_VEMPTY), srow, nullptr,
-                                             abort_flag) &&
+                                             bar(B_VFULL), bar(B_VEMPTY), srow, nullptr, 0u,
+                                             abort_flag, &tmap) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
@@ -554,14 +581,46 @@ int tc_auto_nsplit(int B, int T, int H, int num_sms) {
   return int(ns);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
 cudaError_t init_partial_tc() {
-  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
+  // Contiguous pools are read with TMA box loads (64 rows x 64 columns, 128B
+  // swizzle); the map is encoded on the host for this call's pool.  Paged
+  // calls do not use it.
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof tmap);
+  Params q = p;
+  if (p.kv_start) {
+    bool ok = g_encode != nullptr;
+    if (ok) {
+      cuuint64_t dims[2] = {cuuint64_t(kDqk), cuuint64_t(p.num_slots)};
+      cuuint64_t strides[1] = {cuuint64_t(p.kv_stride) * 2u};
+      cuuint32_t box[2] = {64u, uint32_t(kTile)};
+      cuuint32_t estr[2] = {1u, 1u};
+      ok = g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(p.kv),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (!ok) return cudaErrorNotSupported;
+  }
   dim3 grid(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
-  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(q, tmap);
   return cudaGetLastError();
 }
 

@@ -160,6 +160,23 @@ def test_contiguous_matches_oracle_and_paged(va, path):
     assert torch.equal(out_c, out_p) and torch.equal(lse_c, lse_p)
 
 
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_contiguous_many_tiles_per_split(va, path):
+    """Long splits (dozens of 64-key tiles each) in the contiguous layout,
+    whose whole tiles are read as boxes: the copy ring wraps many times."""
+    s = synth.Spec("contig_long", B=2, H=8, T=16, prefix=[9000, 5000], num_slots=1 << 15,
+                   layout="contiguous", seed=33)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    for ns in (1, 2):
+        ws, _ = va.alloc_workspace(s.B, s.T, s.H, ns, path)
+        out, lse = _gpu.run(va, d, w, path=path, layout="contiguous", nsplit=ns, workspace=ws)
+        assert va.read_status(ws) == 0
+        ref_o, ref_l = _gpu.reference(w)
+        _gpu.compare(out, lse, ref_o, ref_l)
+
+
 def test_tree_bits_input_equals_parents(va):
     w = synth.make(synth.spec("tp8"))
     d = _gpu.to_device(w)
