@@ -10,21 +10,24 @@
 //
 //   QK CTA (cluster rank 0)
 //     TMEM: Q as the A operand (128 lanes x 288 columns of bf16 pairs) and two
-//     64-column S buffers.  Warps 0, 2, 3 gather 64-key tiles with 16-byte
-//     cp.async copies written straight into the 128B-swizzled K-major layout
-//     into 3 stages of 72 KB; warp 1 issues S = Q K^T (36 MMAs of 128x64x16,
-//     A from TMEM, B K-major); warps 4-7 own a row each: read S, mask, online
-//     softmax with a conditional rescale (the reference max only moves when a
-//     tile exceeds it by 2^8), round P to bf16 and store it straight into the
-//     PV CTA's shared memory (distributed shared memory), with the row's
-//     rescale factor.
+//     64-column S buffers.  Warps 0, 2, 3 bring 64-key tiles into 2 stages of
+//     72 KB in the 128B-swizzled K-major layout (16-byte cp.async gathers for
+//     paged keys, TMA boxes for contiguous ones); warp 1 issues S = Q K^T (36
+//     MMAs of 128x64x16, A from TMEM, B K-major); warps 4-11 are two softmax
+//     warpgroups, each owning 32 of a tile's 64 columns for every row: they
+//     share the tile maximum through shared memory, run an online softmax with
+//     a conditional rescale (the reference max only moves when a tile exceeds
+//     it by 2^8), round P to bf16 into a local staging buffer, and one thread
+//     ships P with the rows' rescale factors to the PV CTA with a single
+//     distributed-shared-memory bulk copy.
 //   PV CTA (cluster rank 1)
-//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3 gather the value
+//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3 bring the value
 //     columns (first 512) of the same tiles -- L2 hits behind the QK CTA's
 //     reads -- into 2 stages of 64 KB; warp 1 issues O += P V (8 MMAs of
-//     128x256x16, A = P K-major, B = V MN-major: the gathered tile is K-major
-//     for S and MN-major for PV); warps 4-7 rescale O rows on the rare tiles
-//     whose reference max moved, then normalise and write the split's partial.
+//     128x256x16, A = P K-major, B = V MN-major: the same swizzled tile layout
+//     is K-major for S and MN-major for PV); warps 4-11 rescale O rows on the
+//     rare tiles whose reference max moved, then normalise and write the
+//     split's partial, each warpgroup for 256 of the 512 columns.
 //
 // The design follows the pages' split-K / online-softmax / partial-reduce
 // structure (The Milestone Commit, "The Thinking Process Revealed"; The Commit
@@ -52,7 +55,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kRows = 128;
 constexpr int kTile = 64;                                   // keys per tile
 constexpr int kKBlocks = kDqk / 64;                         // 9 column blocks (K)
@@ -60,25 +63,34 @@ constexpr int kVBlocks = kDv / 64;                          // 8 column blocks (
 constexpr uint32_t kBlockBytes = kTile * 128;               // 8 KB: 64 keys x 64 cols
 constexpr uint32_t kKStageBytes = kKBlocks * kBlockBytes;   // 72 KB
 constexpr uint32_t kVStageBytes = kVBlocks * kBlockBytes;   // 64 KB
-constexpr int kKStages = 3;
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr uint32_t kPBytes = kRows * 128;                   // P tile: 128 rows x 64 keys bf16
+// P buffer: P tile (128 rows x 64 keys bf16, K-major 128B swizzle), then the
+// rows' rescale factors, then the four softmax warps' rescale flags.  Shipped
+// to the PV CTA as one contiguous bulk copy.
+constexpr uint32_t kPBytes = kRows * 128;                   // 16 KB
+constexpr uint32_t kPAlpha = kPBytes;                       // float [128]
+constexpr uint32_t kPFlags = kPAlpha + 4 * kRows;           // uint32 [4]
+constexpr uint32_t kPPayload = kPFlags + 16;                // bytes copied
+constexpr uint32_t kPBufBytes = 17 * 1024;                  // buffer stride (1024-aligned)
+constexpr int kPBufs = 4;                                   // P ring depth (PV CTA)
 
-// shared layout (offsets from a 1024-byte aligned base; identical in both CTAs
-// so that remote addresses and multicast commits land on the right objects)
+// shared layout (offsets from a 1024-byte aligned base; the header is
+// identical in both CTAs so that remote addresses and multicast commits land
+// on the right objects)
 constexpr uint32_t kOffBars = 0;
-constexpr uint32_t kOffTmemSlot = 256;
-constexpr uint32_t kOffAbort = 260;
-constexpr uint32_t kOffCmd = 264;                           // PV: row-warp command word
-constexpr uint32_t kOffFlags = 512;                         // PV: uint32 [2][4] per-warp rescale flags
+constexpr uint32_t kOffTmemSlot = 384;
+constexpr uint32_t kOffAbort = 388;
+constexpr uint32_t kOffCmd = 392;                           // PV: row-warp command word
 constexpr uint32_t kOffValid = 576;                         // QK: uint64 [8] key-validity ring
-constexpr uint32_t kOffAlpha = 1024;                        // PV: float [2][128]
-constexpr uint32_t kOffFin = 2048;                          // PV: float [128]
-constexpr uint32_t kOffSrow = 2560;                         // int32 [3][64] staged pool rows
-constexpr uint32_t kOffK = 4096;                            // QK CTA: K stages
-constexpr uint32_t kOffP = 4096;                            // PV CTA: P buffers
-constexpr uint32_t kOffV = kOffP + 2 * kPBytes;             // PV CTA: V stages
-constexpr uint32_t kEndQK = kOffK + kKStages * kKStageBytes;
+constexpr uint32_t kOffFin = 2048;                          // PV: float [128] 1 / row sum
+constexpr uint32_t kOffSrow = 2560;                         // int32 [2][64] staged pool rows
+constexpr uint32_t kOffMx = 3072;                           // QK: float [2][128] half maxima
+constexpr uint32_t kOffK = 4096;                            // QK: K stages
+constexpr uint32_t kOffStage = kOffK + kKStages * kKStageBytes;   // QK: P staging [2]
+constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
+constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V stages
+constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
 constexpr uint32_t kEndPV = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -89,9 +101,9 @@ constexpr int kValidRing = 8;
 constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
 
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 3, B_SFULL = 6, B_SEMPTY = 8, B_PFREE = 10, B_QREADY = 12,
-  B_MMAFIN = 13, B_VFULL = 14, B_VEMPTY = 16, B_PFULL = 18, B_OGO = 20, B_OCORR = 21,
-  B_ODONE = 22, B_FIN = 23, B_VREADY = 24, kNumBars = 32
+  B_KFULL = 0, B_KEMPTY = 2, B_SFULL = 4, B_SEMPTY = 6, B_PFREE = 8, B_QREADY = 12,
+  B_MMAFIN = 13, B_VFULL = 14, B_VEMPTY = 16, B_PFULL = 18, B_OGO = 22, B_OCORR = 23,
+  B_ODONE = 24, B_FIN = 25, B_VREADY = 26, kNumBars = 34
 };
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
 
@@ -102,6 +114,8 @@ constexpr long long kWaitCycles = 4000000000ll;   // wait bound in SM cycles (~2
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kProducers = 96;        // warps 0, 2, 3
 constexpr uint32_t kProducerBar = 1;  // named barrier of the producer warps
+constexpr int kSoftmax = 256;         // warps 4-11
+constexpr uint32_t kSoftmaxBar = 2;   // named barrier of the softmax warps
 
 // Two probabilities rounded to bf16 for the PV product; the row sum takes the
 // unrounded values so that lse stays exact to fp32 rounding.
@@ -144,7 +158,9 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
     bool got = true;
-    if (t >= kStages)
+    // one thread polls the stage's release; the others learn the outcome at
+    // the named barrier below
+    if (t >= kStages && ptid == 0)
       got = mbar_wait(empty0 + 8u * uint32_t(s), uint32_t((t / kStages) - 1) & 1u, abort_flag,
                       kWaitCycles);
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
@@ -196,30 +212,35 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   return ok;
 }
 
-// Q rows into TMEM as the A operand (bf16 pairs, 288 columns): each softmax
-// thread writes its own row (lane quadrant = warp % 4), 3 column chunks of
-// 32 (64 features each) per round trip to memory.
-__device__ __forceinline__ void load_q(const Params& p, int b, int row0, int warp, int lane,
+// Q rows into TMEM as the A operand (bf16 pairs, 288 columns).  The two
+// softmax warpgroups share the work: warp w writes lane quadrant w%4, column
+// chunks 0-4 (first warpgroup) or 5-8 (second) of 32 columns (64 features
+// each), at most 3 chunks per round trip to memory.
+__device__ __forceinline__ void load_q(const Params& p, int b, int row0, int half, int q4, int lane,
                                        uint32_t tmem) {
-  const int q4 = warp & 3;
   const int lr = row0 + q4 * 32 + lane;
   const bool ok = lr < p.rows_per_req;
   const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t(b) * p.rows_per_req + lr) * kDqk);
   const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + kTmemQ;
+  const int c_begin = half ? 5 : 0, c_end = half ? 9 : 5;
 #pragma unroll 1
-  for (int c0 = 0; c0 < kKBlocks; c0 += 3) {
+  for (int c0 = c_begin; c0 < c_end; c0 += 3) {
+    const int n = c_end - c0 < 3 ? c_end - c0 : 3;
     uint4 buf[24];
 #pragma unroll
-    for (int i = 0; i < 24; ++i) buf[i] = ok ? src[c0 * 8 + i] : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 24; ++i)
+      buf[i] = (ok && i < 8 * n) ? src[c0 * 8 + i] : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int cc = 0; cc < 3; ++cc) {
-      uint32_t v[32];
+      if (cc < n) {
+        uint32_t v[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[4 * i] = buf[cc * 8 + i].x; v[4 * i + 1] = buf[cc * 8 + i].y;
-        v[4 * i + 2] = buf[cc * 8 + i].z; v[4 * i + 3] = buf[cc * 8 + i].w;
+        for (int i = 0; i < 8; ++i) {
+          v[4 * i] = buf[cc * 8 + i].x; v[4 * i + 1] = buf[cc * 8 + i].y;
+          v[4 * i + 2] = buf[cc * 8 + i].z; v[4 * i + 3] = buf[cc * 8 + i].w;
+        }
+        tmem_st32(tl + 32u * uint32_t(c0 + cc), v);
       }
-      tmem_st32(tl + 32u * uint32_t(c0 + cc), v);
     }
   }
   tmem_wait_st();
@@ -254,10 +275,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_OCORR || i == B_QREADY) cnt = 128;
+      if (i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_OCORR || i == B_QREADY) cnt = kSoftmax;
       if (i >= B_KFULL && i < B_KFULL + kKStages) cnt = kProducers + 1;   // copies + producer 0
       if (i >= B_VFULL && i < B_VFULL + kVStages) cnt = kProducers + 1;
-      if (i == B_PFULL || i == B_PFULL + 1 || i == B_FIN) cnt = 4;   // one per softmax warp
+      if (i == B_FIN) cnt = 4;   // one per warp of the first softmax warpgroup
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -270,6 +291,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const bool producer = warp == 0 || warp == 2 || warp == 3;
   const int ptid = warp == 0 ? lane : (warp - 1) * 32 + lane;
   int* srow = reinterpret_cast<int*>(gb + kOffSrow);
+  const int half = (warp - 4) >> 2;   // softmax / row warpgroup (warps >= 4)
+  const int q4 = warp & 3;            // TMEM lane quadrant of the warp
 
   if (rank == 0) {
     // ================================================================ QK CTA
@@ -317,26 +340,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4) {
-      // ---- softmax rows
-      load_q(p, b, row0, warp, lane, tmem);
+      // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of
+      // every tile for row r
+      load_q(p, b, row0, half, q4, lane, tmem);
       tc_fence_before();
       mbar_arrive(bar(B_QREADY));
-      const int q4 = warp & 3;
       const int r = q4 * 32 + lane;
       const int lr = row0 + r;
       const bool row_ok = lr < R;
+      const bool issuer = warp == 4 && lane == 0;
       const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);
       const uint64_t nbits = row_ok ? p.bits[size_t(b) * p.T + lr / p.H] : 0ull;
+      float* mx = reinterpret_cast<float*>(gb + kOffMx);
       const uint32_t pv_p = mapa(sb + kOffP, 1);
-      const uint32_t pv_alpha = mapa(sb + kOffAlpha, 1);
-      const uint32_t pv_flags = mapa(sb + kOffFlags, 1);
-      const uint32_t pv_fin = mapa(sb + kOffFin, 1);
       const uint32_t pv_pfull = mapa(bar(B_PFULL), 1);
+      const uint32_t pv_fin = mapa(sb + kOffFin, 1);
       const uint32_t pv_finbar = mapa(bar(B_FIN), 1);
       float m_ref = -INFINITY, l = 0.f;
+      bool issuer_ok = true;
       bool ok = true;
       for (int t = 0; t < ntiles; ++t) {
-        const int bs = t & 1;
+        const int bs = t & 1;             // S buffer and staging buffer
+        const int pb = t % kPBufs;        // P buffer of the PV CTA
         const int tk0 = sr.k0 + t * kTile;
         // visibility: prefix keys always, draft key k when bit k of the node's mask
         const int off = ri.P - tk0;
@@ -355,29 +380,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait(bar(B_SFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
             mbar_wait(bar(B_VREADY + t % kValidRing), uint32_t(t / kValidRing) & 1u, abort_flag,
                       kWaitCycles);
-        if (!__all_sync(0xffffffffu, got)) {
-          fail();
+        const bool wok = __all_sync(0xffffffffu, got);
+        float x[32];
+        float mth = -INFINITY;
+        if (wok) {
+          const uint32_t v32 = uint32_t(((vis & valid_ring[t % kValidRing]) >> (32 * half)));
+          if (tid == 128) VA_TRACE_EVENT(2, 0, t);
+          tc_fence_after();
+          uint32_t sv[32];
+          tmem_ld32(tl + kTmemS + 64u * uint32_t(bs) + 32u * uint32_t(half), sv);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(B_SEMPTY + bs));
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            x[c] = ((v32 >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+            mth = fmaxf(mth, x[c]);
+          }
+        }
+        mx[half * kRows + r] = mth;
+        if (issuer) bulk_wait_read<1>();   // staging buffer bs: tile t-2's copy has read it
+        if (!named_sync_and(kSoftmaxBar, kSoftmax, wok && issuer_ok)) {
+          if (issuer) fail();
           ok = false;
           break;
         }
-        vis &= valid_ring[t % kValidRing];
-        if (tid == 128) VA_TRACE_EVENT(2, 0, t);
-        tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tl + kTmemS + 64u * uint32_t(bs), s0);
-        tmem_ld32(tl + kTmemS + 64u * uint32_t(bs) + 32u, s1);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY + bs));
-
-        float x[64];
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = ((vis >> c) & 1ull) ? __uint_as_float(s0[c]) * p.scale_log2 : -INFINITY;
-          x[c + 32] = ((vis >> (c + 32)) & 1ull) ? __uint_as_float(s1[c]) * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, fmaxf(x[c], x[c + 32]));
-        }
+        const float mt = fmaxf(mx[r], mx[kRows + r]);
         float alpha = 1.f;
         if (mt > m_ref + kRescaleLog2) {
           alpha = ex2_approx(m_ref - mt);   // 0 when nothing was seen before
@@ -385,45 +413,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_ref = mt;
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < 16; ++c)
           pk[c] = pack_bf16(ex2_approx(x[2 * c] - mr), ex2_approx(x[2 * c + 1] - mr), l);
-        const uint32_t wres = __ballot_sync(0xffffffffu, alpha != 1.f);
         if (tid == 128) VA_TRACE_EVENT(2, 1, t);
-
-        const bool freed = t < 2 || mbar_wait<true>(bar(B_PFREE + bs), uint32_t((t >> 1) - 1) & 1u,
-                                                    abort_flag, kWaitCycles);
-        if (!__all_sync(0xffffffffu, freed)) {
-          fail();
-          ok = false;
-          break;
-        }
-        if (tid == 128) VA_TRACE_EVENT(2, 2, t);
-        const uint32_t prow = pv_p + uint32_t(bs) * kPBytes + uint32_t(r) * 128u;
+        // this row's 32 keys into the staging buffer (K-major, 128B swizzle)
+        uint8_t* stg = gb + kOffStage + uint32_t(bs) * kPBufBytes;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_cluster_v4(prow + uint32_t((j ^ (r & 7)) * 16), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
-                        pk[4 * j + 3]);
-        st_cluster_f32(pv_alpha + uint32_t(bs * 128 + r) * 4u, alpha);
-        if (lane == 0)
-          st_cluster_u32(pv_flags + uint32_t(bs * 4 + q4) * 4u, (uint32_t(t) << 1) | (wres ? 1u : 0u));
-        fence_proxy_async_cluster();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(pv_pfull + 8u * uint32_t(bs));
-        if (tid == 128) VA_TRACE_EVENT(2, 3, t);
+        for (int j = 0; j < 4; ++j) {
+          const int chunk = 4 * half + j;
+          *reinterpret_cast<uint4*>(stg + r * 128 + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+        if (half == 0) {
+          reinterpret_cast<float*>(stg + kPAlpha)[r] = alpha;
+          const uint32_t wres = __ballot_sync(0xffffffffu, alpha != 1.f);
+          if (lane == 0)
+            reinterpret_cast<uint32_t*>(stg + kPFlags)[q4] = (uint32_t(t) << 1) | (wres ? 1u : 0u);
+        }
+        fence_proxy_async_cta();   // staging writes, read by the bulk copy
+        named_sync(kSoftmaxBar, kSoftmax);
+        if (issuer) {
+          issuer_ok = t < kPBufs ||
+                      mbar_wait<true>(bar(B_PFREE + pb), uint32_t((t / kPBufs) - 1) & 1u,
+                                      abort_flag, kWaitCycles);
+          if (tid == 128) VA_TRACE_EVENT(2, 2, t);
+          if (issuer_ok) {
+            // the PV CTA armed this buffer's barrier with the byte count
+            bulk_copy_to_cluster(pv_p + uint32_t(pb) * kPBufBytes, smem_u32(stg), kPPayload,
+                                 pv_pfull + 8u * uint32_t(pb));
+            bulk_commit();
+          }
+          if (tid == 128) VA_TRACE_EVENT(2, 3, t);
+        }
       }
+      // row sums: the two warpgroups' partial sums share the reference max
       if (ok) {
-        const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        if (row_ok) p.part_lse[size_t(split) * rows_total + size_t(b) * R + lr] = lse;
-        st_cluster_f32(pv_fin + uint32_t(r) * 4u, l > 0.f ? 1.f / l : 0.f);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(pv_finbar);
-        // the PV CTA's last releases of our P buffers have landed before we leave
-        for (int t = ntiles - 2 > 0 ? ntiles - 2 : 0; t < ntiles; ++t)
-          if (!mbar_wait<true>(bar(B_PFREE + (t & 1)), uint32_t(t >> 1) & 1u, abort_flag,
-                               kWaitCycles))
-            fail();
+        mx[half * kRows + r] = l;
+        named_sync(kSoftmaxBar, kSoftmax);
+        if (half == 0) {
+          const float lt = mx[r] + mx[kRows + r];
+          const float lse = lt > 0.f ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
+          if (row_ok) p.part_lse[size_t(split) * rows_total + size_t(b) * R + lr] = lse;
+          st_cluster_f32(pv_fin + uint32_t(r) * 4u, lt > 0.f ? 1.f / lt : 0.f);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(pv_finbar);
+        }
+      }
+      if (issuer) {
+        // the last copies have read the staging buffers, and the PV CTA's last
+        // releases of the P buffers have landed, before shared memory goes away
+        bulk_wait_read<0>();
+        if (ok)
+          for (int t = ntiles - kPBufs > 0 ? ntiles - kPBufs : 0; t < ntiles; ++t)
+            if (!mbar_wait<true>(bar(B_PFREE + t % kPBufs), uint32_t(t / kPBufs) & 1u, abort_flag,
+                                 kWaitCycles))
+              fail();
       }
     }
   } else {
@@ -440,21 +486,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- MMA issuer: O += P_t V_t
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_bf16(128, 256, 0, 1);
-        const volatile uint32_t* flags = reinterpret_cast<const volatile uint32_t*>(gb + kOffFlags);
         uint32_t nresc = 0;
         bool ok = true;
+        // each P buffer's barrier expects one arrival (ours, carrying the byte
+        // count of the QK CTA's bulk copy into it): arm the first uses now
+        for (int t = 0; t < kPBufs && t < ntiles; ++t)
+          mbar_arrive_expect_tx(bar(B_PFULL + t), kPPayload);
         for (int t = 0; t < ntiles; ++t) {
-          const int s = t % kVStages, bs = t & 1;
+          const int s = t % kVStages, bs = t % kPBufs;
           if (!mbar_wait(bar(B_VFULL + s), uint32_t(t / kVStages) & 1u, abort_flag, kWaitCycles) ||
-              !mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles)) {
+              !mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t / kPBufs) & 1u, abort_flag,
+                               kWaitCycles)) {
             fail();
             ok = false;
             break;
           }
           VA_TRACE_EVENT(4, 0, t);
+          const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBufBytes;
+          const volatile uint32_t* flags =
+              reinterpret_cast<const volatile uint32_t*>(gb + kOffP + bs * kPBufBytes + kPFlags);
           uint32_t any = 0;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) any |= flags[bs * 4 + w] & 1u;
+          for (int w = 0; w < 4; ++w) any |= flags[w] & 1u;
           if (any && t > 0) {
             // rows change reference: O must be final for tile t-1 before the
             // row warps rescale it, and rescaled before this tile's product
@@ -473,7 +526,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_cta();
           tc_fence_after();
-          const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBytes;
           const uint32_t vbase = sb + kOffV + uint32_t(s) * kVStageBytes;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
@@ -484,6 +536,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             kBlockBytes, 1024, kSwizzle128B);
               mma_ss(tmem + 256u * uint32_t(h), ad, bd, idesc, (t > 0 || k > 0) ? 1u : 0u);
             }
+          // re-arm the buffer for tile t + kPBufs before its release reaches
+          // the QK CTA (the release follows this product's completion)
+          if (t + kPBufs < ntiles) mbar_arrive_expect_tx(bar(B_PFULL + bs), kPPayload);
           mma_commit(bar(B_VEMPTY + s));
           mma_commit_mc(bar(B_PFREE + bs), uint16_t(1u << 0));
           VA_TRACE_EVENT(4, 1, t);
@@ -497,13 +552,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4) {
-      // ---- row warps: rescale O rows on command, then the split's partial
-      const int q4 = warp & 3;
+      // ---- row warps: rescale O rows on command, then the split's partial;
+      // warpgroup `half` owns columns [256*half, 256*half + 256)
       const int r = q4 * 32 + lane;
       const int lr = row0 + r;
       const bool row_ok = lr < R;
-      const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);
-      const float* alpha_s = reinterpret_cast<const float*>(gb + kOffAlpha);
+      const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + 256u * uint32_t(half);
       bool ok = true;
       for (uint32_t k = 0;; ++k) {
         const bool go = mbar_wait(bar(B_OGO), k & 1u, abort_flag, kWaitCycles);
@@ -514,13 +568,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint32_t c = *cmd;
         if (c == kCmdDone) break;
-        const float a = alpha_s[c * 128 + r];
+        const float a = reinterpret_cast<const float*>(gb + kOffP + c * kPBufBytes + kPAlpha)[r];
         tc_fence_after();
         // tcgen05.ld/st are warp-collective: the whole warp takes part when
         // any of its rows rescales, each lane scaling by its own factor
         if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 16; ++cc) {
+          for (int cc = 0; cc < 8; ++cc) {
             uint32_t v[32];
             tmem_ld32(tl + 32u * uint32_t(cc), v);
             tmem_wait_ld();
@@ -538,9 +592,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (__all_sync(0xffffffffu, fin)) {
         tc_fence_after();
         const float inv = reinterpret_cast<const float*>(gb + kOffFin)[r];
-        float* dst = p.part_o + (size_t(split) * rows_total + size_t(b) * R + lr) * kDv;
+        float* dst = p.part_o + (size_t(split) * rows_total + size_t(b) * R + lr) * kDv + 256 * half;
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 8; ++c) {
           uint32_t v[32];
           tmem_ld32(tl + 32u * uint32_t(c), v);
           tmem_wait_ld();
