@@ -121,8 +121,8 @@ constexpr uint32_t kSoftmaxBar = 2;   // named barrier of the softmax warps
 // unrounded values so that lse stays exact to fp32 rounding.
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sum) {
   sum += a + b;
-  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // a in the low half
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Pool row of key j of the split, or -1 when j is past the split or has no
@@ -139,8 +139,11 @@ __device__ __forceinline__ int key_row_or_none(const Params& p, const ReqInfo& r
 //  - Paged keys, or a split's ragged last tile: 16-byte cp.async copies from
 //    every producer thread (zero-filled for keys without a row).  The tile's
 //    pool rows are staged in shared memory and fetched one tile ahead.
-//  - Contiguous keys (kv_start) for a whole in-range tile: one TMA tiled box
-//    load of 64 rows x 64 columns per column block.
+//  - Contiguous keys (kv_start) for a whole in-range tile: TMA tiled box
+//    loads.  With a 3-D map (column-in-block, pool row, column block) one box
+//    of 64 columns x 64 rows x all column blocks lands the whole tile in the
+//    staged layout with a single instruction; otherwise one 64 x 64 box per
+//    column block.
 // With kMask the tile's 64-bit key-validity mask goes to the ring read by the
 // softmax warps.  Completion: every producer's cp.async arrival (noinc) plus
 // one arrival of producer 0 (with the TMA byte count when boxes are used,
@@ -151,7 +154,8 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
                                         int ntiles, int ptid, uint32_t stage_base,
                                         uint32_t stage_bytes, uint32_t full0, uint32_t empty0,
                                         int* srow, uint32_t* valid32, uint32_t vready0,
-                                        volatile int* abort_flag, const CUtensorMap* tmap) {
+                                        volatile int* abort_flag, const CUtensorMap* tmap,
+                                        bool box3d) {
   const int lane = ptid & 31;
   int rw = ptid < 64 ? key_row_or_none(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
@@ -187,23 +191,37 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     if (ptid == 0) {
       if (boxes) {
         mbar_arrive_expect_tx(full0 + 8u * uint32_t(s), uint32_t(kChunks / 8) * kBlockBytes);
+        if (box3d) {
+          tma_load_3d(dst0, tmap, 0, int(row0), 0, full0 + 8u * uint32_t(s));
+        } else {
 #pragma unroll 1
-        for (int c = 0; c < kChunks / 8; ++c)
-          tma_load_2d(dst0 + uint32_t(c) * kBlockBytes, tmap, 64 * c, int(row0),
-                      full0 + 8u * uint32_t(s));
+          for (int c = 0; c < kChunks / 8; ++c)
+            tma_load_2d(dst0 + uint32_t(c) * kBlockBytes, tmap, 64 * c, int(row0),
+                        full0 + 8u * uint32_t(s));
+        }
       } else {
         mbar_arrive(full0 + 8u * uint32_t(s));
       }
     }
     if (ptid < 64 && t + 1 < ntiles) rw = key_row_or_none(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
-#pragma unroll 4
-    for (int idx = ptid; !boxes && idx < 64 * kChunks; idx += kProducers) {
-      const int key = idx / kChunks, c = idx - key * kChunks;
-      const int row = srow[s * 64 + key];
-      const __nv_bfloat16* src = row >= 0 ? p.kv + int64_t(row) * p.kv_stride + c * 8 : p.kv;
-      const uint32_t dst = dst0 + uint32_t(c >> 3) * kBlockBytes + uint32_t(key) * 128u +
-                           uint32_t(((c & 7) ^ (key & 7)) * 16);
-      cp_async16(dst, src, row >= 0 ? 16u : 0u);
+    if (!boxes) {
+      // warp per key: lane l copies 16-byte chunks l, l+32, l+64 of the row,
+      // so one warp instruction moves 512 contiguous bytes
+      const int pw = ptid >> 5;
+#pragma unroll 2
+      for (int key = pw; key < kTile; key += kProducers / 32) {
+        const int row = srow[s * 64 + key];
+        const __nv_bfloat16* src = p.kv + (row >= 0 ? int64_t(row) * p.kv_stride : 0);
+        const uint32_t nb = row >= 0 ? 16u : 0u;
+        const uint32_t kd = dst0 + uint32_t(key) * 128u;
+#pragma unroll
+        for (int j = 0; j < (kChunks + 31) / 32; ++j) {
+          const int c = lane + 32 * j;
+          if (c < kChunks)
+            cp_async16(kd + uint32_t(c >> 3) * kBlockBytes + uint32_t(((c & 7) ^ (key & 7)) * 16),
+                       src + c * 8, nb);
+        }
+      }
     }
     cp_async_arrive_noinc(full0 + 8u * uint32_t(s));
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
@@ -247,7 +265,8 @@ __device__ __forceinline__ void load_q(const Params& p, int b, int row0, int hal
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    partial_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap) {
+    partial_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, int box3d) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -285,6 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) tmem_alloc(sb + kOffTmemSlot, kTmemCols);
+  if (tid == 0 && p.kv_start) tma_prefetch(rank == 0 ? &tmap_k : &tmap_v);
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
@@ -302,42 +322,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!produce<kDqk / 8, kKStages, true>(p, ri, sr, ntiles, ptid, sb + kOffK, kKStageBytes,
                                              bar(B_KFULL), bar(B_KEMPTY), srow,
                                              reinterpret_cast<uint32_t*>(gb + kOffValid),
-                                             bar(B_VREADY), abort_flag, &tmap) &&
+                                             bar(B_VREADY), abort_flag, &tmap_k, box3d != 0) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
-      // ---- MMA issuer: S[t%2] = Q K_t^T
-      if (lane == 0) {
-        bool ok = mbar_wait(bar(B_QREADY), 0, abort_flag, kWaitCycles);
-        if (!ok) fail();
-        constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
-        for (int t = 0; ok && t < ntiles; ++t) {
-          const int s = t % kKStages, bs = t & 1;
-          if (!mbar_wait(bar(B_KFULL + s), uint32_t(t / kKStages) & 1u, abort_flag, kWaitCycles) ||
-              (t >= 2 && !mbar_wait(bar(B_SEMPTY + bs), uint32_t((t >> 1) - 1) & 1u, abort_flag,
-                                    kWaitCycles))) {
-            fail();
-            break;
-          }
-          fence_proxy_async_cta();   // the producers' cp.async writes, seen by the tensor core
-          tc_fence_after();
-          VA_TRACE_EVENT(1, 0, t);
-          const uint32_t kbase = sb + kOffK + uint32_t(s) * kKStageBytes;
-          const uint32_t d = tmem + kTmemS + 64u * uint32_t(bs);
-#pragma unroll 4
-          for (int k = 0; k < kDqk / 16; ++k) {
-            const uint64_t bd =
-                smem_desc(kbase + uint32_t(k >> 2) * kBlockBytes + uint32_t(k & 3) * 32u, 16, 1024,
-                          kSwizzle128B);
-            mma_ts(d, tmem + kTmemQ + 8u * uint32_t(k), bd, idesc, k > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SFULL + bs));
-          mma_commit(bar(B_KEMPTY + s));
-          VA_TRACE_EVENT(1, 1, t);
+      // ---- MMA issuer: S[t%2] = Q K_t^T.  The whole warp runs the loop and
+      // one elected lane issues, 36 MMAs back to back with fixed descriptor
+      // offsets, so the tensor pipe sees them at its own rate.
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QREADY), 0, abort_flag, kWaitCycles));
+      if (!ok && lane == 0) fail();
+      constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % kKStages, bs = t & 1;
+        const bool got =
+            mbar_wait(bar(B_KFULL + s), uint32_t(t / kKStages) & 1u, abort_flag, kWaitCycles) &&
+            (t < 2 || mbar_wait(bar(B_SEMPTY + bs), uint32_t((t >> 1) - 1) & 1u, abort_flag,
+                                kWaitCycles));
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) fail();
+          break;
         }
-        mma_commit(bar(B_MMAFIN));
-        mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
+        fence_proxy_async_cta();   // the producers' cp.async writes, seen by the tensor core
+        tc_fence_after();
+        if (lane == 0) VA_TRACE_EVENT(1, 0, t);
+        const uint64_t bd0 =
+            smem_desc(sb + kOffK + uint32_t(s) * kKStageBytes, 16, 1024, kSwizzle128B);
+        const uint32_t d = tmem + kTmemS + 64u * uint32_t(bs);
+        // K columns 16k..16k+15: column block k/4, 32-byte step k%4 inside the
+        // swizzled row (the descriptor's address field counts 16-byte units)
+#pragma unroll
+        for (int k = 0; k < kDqk / 16; ++k)
+          mma_ts_warp(d, tmem + kTmemQ + 8u * uint32_t(k),
+                      bd0 + uint64_t((uint32_t(k >> 2) * kBlockBytes + uint32_t(k & 3) * 32u) >> 4),
+                      idesc, k > 0 ? 1u : 0u);
+        mma_commit_warp(bar(B_SFULL + bs));
+        mma_commit_warp(bar(B_KEMPTY + s));
+        if (lane == 0) VA_TRACE_EVENT(1, 1, t);
       }
+      mma_commit_warp(bar(B_MMAFIN));
+      mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
       __syncwarp();
     } else if (warp >= 4) {
       // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of
@@ -479,77 +502,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- producers: value columns of the same tiles
       if (!produce<kDv / 8, kVStages, false>(p, ri, sr, ntiles, ptid, sb + kOffV, kVStageBytes,
                                              bar(B_VFULL), bar(B_VEMPTY), srow, nullptr, 0u,
-                                             abort_flag, &tmap) &&
+                                             abort_flag, &tmap_v, box3d != 0) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
-      // ---- MMA issuer: O += P_t V_t
-      if (lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16(128, 256, 0, 1);
-        uint32_t nresc = 0;
-        bool ok = true;
-        // each P buffer's barrier expects one arrival (ours, carrying the byte
-        // count of the QK CTA's bulk copy into it): arm the first uses now
+      // ---- MMA issuer: O += P_t V_t (whole warp, one elected lane issues)
+      constexpr uint32_t idesc = idesc_bf16(128, 256, 0, 1);
+      uint32_t nresc = 0;
+      // each P buffer's barrier expects one arrival (ours, carrying the byte
+      // count of the QK CTA's bulk copy into it): arm the first uses now
+      if (lane == 0)
         for (int t = 0; t < kPBufs && t < ntiles; ++t)
           mbar_arrive_expect_tx(bar(B_PFULL + t), kPPayload);
-        for (int t = 0; t < ntiles; ++t) {
-          const int s = t % kVStages, bs = t % kPBufs;
-          if (!mbar_wait(bar(B_VFULL + s), uint32_t(t / kVStages) & 1u, abort_flag, kWaitCycles) ||
-              !mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t / kPBufs) & 1u, abort_flag,
-                               kWaitCycles)) {
-            fail();
-            ok = false;
-            break;
-          }
-          VA_TRACE_EVENT(4, 0, t);
-          const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBufBytes;
-          const volatile uint32_t* flags =
-              reinterpret_cast<const volatile uint32_t*>(gb + kOffP + bs * kPBufBytes + kPFlags);
-          uint32_t any = 0;
+      __syncwarp();
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kVStages, bs = t % kPBufs;
+        const bool got =
+            mbar_wait(bar(B_VFULL + s), uint32_t(t / kVStages) & 1u, abort_flag, kWaitCycles) &&
+            mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t / kPBufs) & 1u, abort_flag, kWaitCycles);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) fail();
+          break;
+        }
+        if (lane == 0) VA_TRACE_EVENT(4, 0, t);
+        const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBufBytes;
+        const volatile uint32_t* flags =
+            reinterpret_cast<const volatile uint32_t*>(gb + kOffP + bs * kPBufBytes + kPFlags);
+        uint32_t any = 0;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) any |= flags[w] & 1u;
-          if (any && t > 0) {
-            // rows change reference: O must be final for tile t-1 before the
-            // row warps rescale it, and rescaled before this tile's product
-            mma_commit(bar(B_ODONE));
-            ok = mbar_wait(bar(B_ODONE), nresc & 1u, abort_flag, kWaitCycles);
-            if (ok) {
+        for (int w = 0; w < 4; ++w) any |= flags[w] & 1u;
+        if (__any_sync(0xffffffffu, any != 0) && t > 0) {
+          // rows change reference: O must be final for tile t-1 before the
+          // row warps rescale it, and rescaled before this tile's product
+          mma_commit_warp(bar(B_ODONE));
+          bool g = __all_sync(0xffffffffu,
+                              mbar_wait(bar(B_ODONE), nresc & 1u, abort_flag, kWaitCycles));
+          if (g) {
+            if (lane == 0) {
               *cmd = uint32_t(bs);
               mbar_arrive(bar(B_OGO));
-              ok = mbar_wait(bar(B_OCORR), nresc & 1u, abort_flag, kWaitCycles);
             }
-            ++nresc;
-            if (!ok) {
-              fail();
-              break;
-            }
+            __syncwarp();
+            g = __all_sync(0xffffffffu,
+                           mbar_wait(bar(B_OCORR), nresc & 1u, abort_flag, kWaitCycles));
           }
-          fence_proxy_async_cta();
-          tc_fence_after();
-          const uint32_t vbase = sb + kOffV + uint32_t(s) * kVStageBytes;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k) {
-              const uint64_t ad = smem_desc(pbase + uint32_t(k) * 32u, 16, 1024, kSwizzle128B);
-              const uint64_t bd = smem_desc(vbase + uint32_t(4 * h) * kBlockBytes + uint32_t(k) * 2048u,
-                                            kBlockBytes, 1024, kSwizzle128B);
-              mma_ss(tmem + 256u * uint32_t(h), ad, bd, idesc, (t > 0 || k > 0) ? 1u : 0u);
-            }
-          // re-arm the buffer for tile t + kPBufs before its release reaches
-          // the QK CTA (the release follows this product's completion)
-          if (t + kPBufs < ntiles) mbar_arrive_expect_tx(bar(B_PFULL + bs), kPPayload);
-          mma_commit(bar(B_VEMPTY + s));
-          mma_commit_mc(bar(B_PFREE + bs), uint16_t(1u << 0));
-          VA_TRACE_EVENT(4, 1, t);
+          ++nresc;
+          if (!g) {
+            if (lane == 0) fail();
+            break;
+          }
         }
-        // last command to the row warps: no more rescales
+        fence_proxy_async_cta();
+        tc_fence_after();
+        const uint64_t ad0 = smem_desc(pbase, 16, 1024, kSwizzle128B);
+        const uint64_t bd0 =
+            smem_desc(sb + kOffV + uint32_t(s) * kVStageBytes, kBlockBytes, 1024, kSwizzle128B);
+        // O columns [256h, 256h+256) += P keys 16k..16k+15 x V rows of those
+        // keys: A steps 32 bytes inside P's swizzled rows, B steps two 8-key
+        // groups (2 KB) down the value tile, whose column blocks 4h..4h+3
+        // form the 256-wide N extent (8 KB apart)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ss_warp(tmem + 256u * uint32_t(h), ad0 + uint64_t((uint32_t(k) * 32u) >> 4),
+                        bd0 + uint64_t((uint32_t(4 * h) * kBlockBytes + uint32_t(k) * 2048u) >> 4),
+                        idesc, (t > 0 || k > 0) ? 1u : 0u);
+        // re-arm the buffer for tile t + kPBufs before its release reaches
+        // the QK CTA (the release follows this product's completion)
+        if (lane == 0 && t + kPBufs < ntiles) mbar_arrive_expect_tx(bar(B_PFULL + bs), kPPayload);
+        __syncwarp();
+        mma_commit_warp(bar(B_VEMPTY + s));
+        mma_commit_mc_warp(bar(B_PFREE + bs), uint16_t(1u << 0));
+        if (lane == 0) VA_TRACE_EVENT(4, 1, t);
+      }
+      // last command to the row warps: no more rescales
+      if (lane == 0) {
         *cmd = kCmdDone;
         mbar_arrive(bar(B_OGO));
-        mma_commit(bar(B_MMAFIN));
-        mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
-        (void)ok;
       }
+      __syncwarp();
+      mma_commit_warp(bar(B_MMAFIN));
+      mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
       __syncwarp();
     } else if (warp >= 4) {
       // ---- row warps: rescale O rows on command, then the split's partial;
@@ -652,29 +686,48 @@ cudaError_t init_partial_tc() {
   return cudaSuccess;
 }
 
-cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
-  // Contiguous pools are read with TMA box loads (64 rows x 64 columns, 128B
-  // swizzle); the map is encoded on the host for this call's pool.  Paged
-  // calls do not use it.
-  CUtensorMap tmap;
-  memset(&tmap, 0, sizeof tmap);
-  Params q = p;
-  if (p.kv_start) {
-    bool ok = g_encode != nullptr;
-    if (ok) {
-      cuuint64_t dims[2] = {cuuint64_t(kDqk), cuuint64_t(p.num_slots)};
-      cuuint64_t strides[1] = {cuuint64_t(p.kv_stride) * 2u};
-      cuuint32_t box[2] = {64u, uint32_t(kTile)};
-      cuuint32_t estr[2] = {1u, 1u};
-      ok = g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(p.kv),
-                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+// Tensor maps of a contiguous pool: 3-D (64 columns, pool rows, column
+// blocks: strides one row and 128 bytes) so that one box of depth `blocks`
+// covers a whole 64-key tile; 2-D (576 columns, pool rows) as the fallback.
+bool encode_pool_map(CUtensorMap* m, const Params& p, int blocks) {
+  if (blocks > 0) {
+    cuuint64_t dims[3] = {64u, cuuint64_t(p.num_slots), cuuint64_t(kKBlocks)};
+    cuuint64_t strides[2] = {cuuint64_t(p.kv_stride) * 2u, 128u};
+    cuuint32_t box[3] = {64u, uint32_t(kTile), uint32_t(blocks)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(p.kv), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  cuuint64_t dims[2] = {cuuint64_t(kDqk), cuuint64_t(p.num_slots)};
+  cuuint64_t strides[1] = {cuuint64_t(p.kv_stride) * 2u};
+  cuuint32_t box[2] = {64u, uint32_t(kTile)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(p.kv), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
+  // Contiguous pools are read with TMA box loads; the maps are encoded on the
+  // host for this call's pool.  Paged calls do not use them.
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof tk);
+  memset(&tv, 0, sizeof tv);
+  int box3d = 0;
+  if (p.kv_start) {
+    if (!g_encode) return cudaErrorNotSupported;
+    if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) {
+      box3d = 1;
+    } else {
+      if (!encode_pool_map(&tk, p, 0)) return cudaErrorNotSupported;
+      tv = tk;
     }
-    if (!ok) return cudaErrorNotSupported;
   }
   dim3 grid(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
-  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(q, tmap);
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv, box3d);
   return cudaGetLastError();
 }
 
