@@ -48,7 +48,35 @@ def parse():
     ap.add_argument("--nsplit", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", default="",
+                    help="H,prefix,layout: run only --warmup + --steps plain calls of that "
+                         "workload (the small captures the ncu summaries are made from); "
+                         "prints a timing note, not the benchmark line")
     return ap.parse_args()
+
+
+def run_case(va, args, dev):
+    """A few plain verify calls of one workload, for profiler captures."""
+    H, P, layout = args.case.split(",")
+    H, P = int(H), int(P)
+    rows = 1 << 18
+    while rows < 2 * (P + 16):
+        rows *= 2
+    pool = device_pool(rows, seed=1, dev=dev)
+    st = Step(va, pool, H, 16, P, seed=7, nrot=2, dev=dev, path=args.path, nsplit=args.nsplit,
+              layout=layout)
+    for k in range(args.warmup):
+        st.call(k)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for k in range(args.steps):
+        st.call(k)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / max(1, args.steps) * 1e3
+    print(f"case H={H} P={P} {layout} nsplit={st.nsplit}: {us:.2f} us/call "
+          f"(eager launches, not the benchmark figure)", flush=True)
 
 
 def dist_env():
@@ -345,6 +373,9 @@ def main():
     import mla_speculative_decode_gb300 as va
     va.build()
     va.init(local)
+    if args.case:
+        run_case(va, args, dev)
+        return
     hbm_peak, tc_peak, peak_kind = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 

@@ -61,20 +61,43 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
   return ok != 0;
 }
 
+// Potentially suspending phase test: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or a system-dependent time
+// limit passes, instead of spinning on the issue slots its neighbours need.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+      "%2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity`: gives up after
 // `limit_cycles` SM clock cycles (or once *abort is set) and returns false;
-// it never spins forever.
+// it never waits forever (each try_wait returns within the hardware's
+// suspend limit, and the clock is read after every unsuccessful try).
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           long long limit_cycles) {
   if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (abort && *abort) return false;
-      if (clock64() - t0 > limit_cycles) return false;
-    }
+  for (;;) {
+    if (kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   }
 }
 

@@ -10,7 +10,7 @@
 //
 //   QK CTA (cluster rank 0)
 //     TMEM: Q as the A operand (128 lanes x 288 columns of bf16 pairs) and two
-//     64-column S buffers.  Warps 0, 2, 3 bring 64-key tiles into 2 stages of
+//     64-column S buffers.  Warps 0, 2, 3, 12-15 bring 64-key tiles into 2 stages of
 //     72 KB in the 128B-swizzled K-major layout (16-byte cp.async gathers for
 //     paged keys, TMA boxes for contiguous ones); warp 1 issues S = Q K^T (36
 //     MMAs of 128x64x16, A from TMEM, B K-major); warps 4-11 are two softmax
@@ -21,7 +21,7 @@
 //     ships P with the rows' rescale factors to the PV CTA with a single
 //     distributed-shared-memory bulk copy.
 //   PV CTA (cluster rank 1)
-//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3 bring the value
+//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3, 12-15 bring the value
 //     columns (first 512) of the same tiles -- L2 hits behind the QK CTA's
 //     reads -- into 2 stages of 64 KB; warp 1 issues O += P V (8 MMAs of
 //     128x256x16, A = P K-major, B = V MN-major: the same swizzled tile layout
@@ -55,7 +55,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kRows = 128;
 constexpr int kTile = 64;                                   // keys per tile
 constexpr int kKBlocks = kDqk / 64;                         // 9 column blocks (K)
@@ -112,7 +112,7 @@ constexpr uint32_t kTmemQ = 0;      // QK CTA: Q, 288 columns
 constexpr uint32_t kTmemS = 320;    // QK CTA: S buffers at 320 and 384
 constexpr long long kWaitCycles = 4000000000ll;   // wait bound in SM cycles (~2 s)
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kProducers = 96;        // warps 0, 2, 3
+constexpr int kProducers = 224;       // warps 0, 2, 3, 12-15
 constexpr uint32_t kProducerBar = 1;  // named barrier of the producer warps
 constexpr int kSoftmax = 256;         // warps 4-11
 constexpr uint32_t kSoftmaxBar = 2;   // named barrier of the softmax warps
@@ -125,15 +125,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sum) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Pool row of key j of the split, or -1 when j is past the split or has no
-// valid slot (its copy then zero-fills).
-__device__ __forceinline__ int key_row_or_none(const Params& p, const ReqInfo& ri, int j, int k1) {
-  if (j >= k1) return -1;
-  const int64_t r = key_row(p, ri, j);
-  return r >= 0 ? int(r) : -1;
+// Raw pool row of key j of the split as stored in the slot list (contiguous
+// pools: the row itself), or -1 when j is past the split or the list.  The
+// value is only range-checked when it is used, a tile later, so the load's
+// latency overlaps the current tile's copies instead of stalling the warp.
+__device__ __forceinline__ int fetch_row(const Params& p, const ReqInfo& ri, int j, int k1) {
+  if (j >= k1 || j >= ri.nlist) return -1;
+  if (p.kv_start) {
+    const int64_t r = ri.base + j;
+    return (r >= 0 && r < p.num_slots && r <= 0x7fffffff) ? int(r) : -1;
+  }
+  return __ldg(p.slot_idx + ri.base + j);
+}
+// A fetched row, or -1 (no row: the copy zero-fills) when out of the pool.
+__device__ __forceinline__ int checked_row(const Params& p, int raw) {
+  return (raw >= 0 && int64_t(raw) < p.num_slots) ? raw : -1;
 }
 
-// Producer warps (96 threads): bring each 64-key tile into the stage ring in
+// Producer warps (224 threads): bring each 64-key tile into the stage ring in
 // the 128B-swizzled K-major layout (column block c/8, row `key`, 16-byte
 // chunk (c%8) ^ (key%8)).
 //  - Paged keys, or a split's ragged last tile: 16-byte cp.async copies from
@@ -157,7 +166,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
                                         volatile int* abort_flag, const CUtensorMap* tmap,
                                         bool box3d) {
   const int lane = ptid & 31;
-  int rw = ptid < 64 ? key_row_or_none(p, ri, sr.k0 + ptid, sr.k1) : -1;
+  int raw = ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
@@ -169,6 +178,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
                       kWaitCycles);
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
     if (ptid < 64) {
+      const int rw = checked_row(p, raw);
       srow[s * 64 + ptid] = rw;
       if (kMask) {
         const int j = sr.k0 + t * kTile + ptid;
@@ -203,7 +213,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
         mbar_arrive(full0 + 8u * uint32_t(s));
       }
     }
-    if (ptid < 64 && t + 1 < ntiles) rw = key_row_or_none(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
+    if (ptid < 64 && t + 1 < ntiles) raw = fetch_row(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
     if (!boxes) {
       // warp per key: lane l copies 16-byte chunks l, l+32, l+64 of the row,
       // so one warp instruction moves 512 contiguous bytes
@@ -308,8 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
-  const bool producer = warp == 0 || warp == 2 || warp == 3;
-  const int ptid = warp == 0 ? lane : (warp - 1) * 32 + lane;
+  const bool producer = warp == 0 || warp == 2 || warp == 3 || warp >= 12;
+  const int ptid = warp == 0 ? lane : (warp < 4 ? warp - 1 : warp - 9) * 32 + lane;
   int* srow = reinterpret_cast<int*>(gb + kOffSrow);
   const int half = (warp - 4) >> 2;   // softmax / row warpgroup (warps >= 4)
   const int q4 = warp & 3;            // TMEM lane quadrant of the warp
