@@ -10,24 +10,26 @@
 //
 //   QK CTA (cluster rank 0)
 //     TMEM: Q as the A operand (128 lanes x 288 columns of bf16 pairs) and two
-//     64-column S buffers.  Warps 0, 2, 3, 12-15 bring 64-key tiles into 2 stages of
-//     72 KB in the 128B-swizzled K-major layout (16-byte cp.async gathers for
-//     paged keys, TMA boxes for contiguous ones); warp 1 issues S = Q K^T (36
-//     MMAs of 128x64x16, A from TMEM, B K-major); warps 4-11 are two softmax
-//     warpgroups, each owning 32 of a tile's 64 columns for every row: they
-//     share the tile maximum through shared memory, run an online softmax with
-//     a conditional rescale (the reference max only moves when a tile exceeds
-//     it by 2^8), round P to bf16 into a local staging buffer, and one thread
-//     ships P with the rows' rescale factors to the PV CTA with a single
+//     64-column S buffers.  Warps 0, 2, 3, 12-15 bring 64-key tiles into a
+//     ring of 23 slots of 8 KB, one 64-column block of a tile per slot, in the
+//     128B-swizzled K-major layout (16-byte cp.async gathers for paged keys,
+//     TMA boxes for contiguous ones); warp 1 issues S = Q K^T (36 MMAs of
+//     128x64x16, A from TMEM, B K-major) and releases each slot as soon as its
+//     four products are done; warps 4-11 are two softmax warpgroups, each
+//     owning 32 of a tile's 64 columns for every row: they share the tile
+//     maximum through shared memory, run an online softmax with a conditional
+//     rescale (the reference max only moves when a tile exceeds it by 2^8),
+//     round P to bf16 into a local staging buffer, and one thread ships P with
+//     the rows' rescale factors to the PV CTA with a single
 //     distributed-shared-memory bulk copy.
 //   PV CTA (cluster rank 1)
-//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3, 12-15 bring the value
-//     columns (first 512) of the same tiles -- L2 hits behind the QK CTA's
-//     reads -- into 2 stages of 64 KB; warp 1 issues O += P V (8 MMAs of
-//     128x256x16, A = P K-major, B = V MN-major: the same swizzled tile layout
-//     is K-major for S and MN-major for PV); warps 4-11 rescale O rows on the
-//     rare tiles whose reference max moved, then normalise and write the
-//     split's partial, each warpgroup for 256 of the 512 columns.
+//     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3, 12-15 bring the
+//     value columns (first 512) of the same tiles -- L2 hits behind the QK
+//     CTA's reads -- into a ring of 16 slots; warp 1 issues O += P V (8 MMAs
+//     of 128x256x16, A = P K-major, B = V MN-major: the same swizzled block
+//     layout is K-major for S and MN-major for PV); warps 4-11 rescale O rows
+//     on the rare tiles whose reference max moved, then normalise and write
+//     the split's partial, each warpgroup for 256 of the 512 columns.
 //
 // The design follows the pages' split-K / online-softmax / partial-reduce
 // structure (The Milestone Commit, "The Thinking Process Revealed"; The Commit
@@ -61,10 +63,20 @@ constexpr int kTile = 64;                                   // keys per tile
 constexpr int kKBlocks = kDqk / 64;                         // 9 column blocks (K)
 constexpr int kVBlocks = kDv / 64;                          // 8 column blocks (V)
 constexpr uint32_t kBlockBytes = kTile * 128;               // 8 KB: 64 keys x 64 cols
-constexpr uint32_t kKStageBytes = kKBlocks * kBlockBytes;   // 72 KB
-constexpr uint32_t kVStageBytes = kVBlocks * kBlockBytes;   // 64 KB
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+// Keys and values stream through rings of 8 KB slots, one column block of a
+// 64-key tile per slot: tile t's block c occupies slot (nb*t + c) mod R
+// (nb = 9 for K, 8 for V).  Each slot has its own release barrier, committed
+// after the MMAs that read it, so the next tiles start loading while the
+// current tile's products are still running, and the ring holds more than two
+// tiles.  The value ring size is a multiple of 4 so that each group of four
+// value blocks (the 256-column N extent of one PV product) sits in adjacent
+// slots: with A = P read from shared memory, a 256-wide product reads 12 KB
+// of shared memory per 128 cycles, a 128-wide one 8 KB per 64 cycles, more
+// than the shared memory can deliver next to the incoming copies.
+constexpr int kRingK = 23;
+constexpr int kRingV = 16;
+constexpr int kVGroup = 4;                                  // value blocks per PV product
+static_assert(kRingV % kVGroup == 0 && kRingK >= 2 * kKBlocks && kRingV >= 2 * kVBlocks, "rings");
 // P buffer: P tile (128 rows x 64 keys bf16, K-major 128B swizzle), then the
 // rows' rescale factors, then the four softmax warps' rescale flags.  Shipped
 // to the PV CTA as one contiguous bulk copy.
@@ -74,38 +86,48 @@ constexpr uint32_t kPFlags = kPAlpha + 4 * kRows;           // uint32 [4]
 constexpr uint32_t kPPayload = kPFlags + 16;                // bytes copied
 constexpr uint32_t kPBufBytes = 17 * 1024;                  // buffer stride (1024-aligned)
 constexpr int kPBufs = 4;                                   // P ring depth (PV CTA)
-
-// shared layout (offsets from a 1024-byte aligned base; the header is
-// identical in both CTAs so that remote addresses and multicast commits land
-// on the right objects)
-constexpr uint32_t kOffBars = 0;
-constexpr uint32_t kOffTmemSlot = 384;
-constexpr uint32_t kOffAbort = 388;
-constexpr uint32_t kOffCmd = 392;                           // PV: row-warp command word
-constexpr uint32_t kOffValid = 576;                         // QK: uint64 [8] key-validity ring
-constexpr uint32_t kOffFin = 2048;                          // PV: float [128] 1 / row sum
-constexpr uint32_t kOffSrow = 2560;                         // int32 [2][64] staged pool rows
-constexpr uint32_t kOffMx = 3072;                           // QK: float [2][128] half maxima
-constexpr uint32_t kOffK = 4096;                            // QK: K stages
-constexpr uint32_t kOffStage = kOffK + kKStages * kKStageBytes;   // QK: P staging [2]
-constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
-constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V stages
-constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
-constexpr uint32_t kEndPV = kOffV + kVStages * kVStageBytes;
-constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-// Key-validity masks travel through their own ring of 8 barriers: the
-// producers run at most kKStages + 2 tiles ahead of the softmax warps, so a
-// parity wait on this ring is never two phases behind.
 constexpr int kValidRing = 8;
 constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
 
+// Barriers.  The header layout is identical in both CTAs so that remote
+// arrivals and multicast commits land on the right objects.
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 2, B_SFULL = 4, B_SEMPTY = 6, B_PFREE = 8, B_QREADY = 12,
-  B_MMAFIN = 13, B_VFULL = 14, B_VEMPTY = 16, B_PFULL = 18, B_OGO = 22, B_OCORR = 23,
-  B_ODONE = 24, B_FIN = 25, B_VREADY = 26, kNumBars = 34
+  B_FULL = 0,                 // [2] tile landed (K in the QK CTA, V in the PV CTA)
+  B_EMPTY = 2,                // [kRingK] slot released by the MMAs that read it
+  B_SFULL = B_EMPTY + kRingK, // [2]
+  B_SEMPTY = B_SFULL + 2,     // [2]
+  B_PFREE = B_SEMPTY + 2,     // [kPBufs] (QK CTA; committed by the PV CTA)
+  B_PFULL = B_PFREE + kPBufs, // [kPBufs] (PV CTA; bulk copies from the QK CTA)
+  B_QREADY = B_PFULL + kPBufs,
+  B_MMAFIN, B_OGO, B_OCORR, B_ODONE, B_FIN,
+  B_VREADY,                   // [kValidRing] key-validity masks (QK CTA)
+  kNumBars = B_VREADY + kValidRing
 };
+
+// shared layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffBars = 0;
+constexpr uint32_t kOffTmemSlot = 512;
+constexpr uint32_t kOffAbort = 516;
+constexpr uint32_t kOffCmd = 520;                           // PV: row-warp command word
+constexpr uint32_t kOffValid = 576;                         // QK: uint64 [8] key-validity ring
+constexpr uint32_t kOffFin = 1024;                          // PV: float [128] 1 / row sum
+constexpr uint32_t kOffSrow = 1536;                         // int32 [2][64] staged pool rows
+constexpr uint32_t kOffMx = 2048;                           // QK: float [2][128] half maxima
+constexpr uint32_t kOffK = 4096;                            // QK: K ring
+constexpr uint32_t kOffStage = kOffK + kRingK * kBlockBytes;   // QK: P staging [2]
+constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
+constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V ring
+constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
+constexpr uint32_t kEndPV = kOffV + kRingV * kBlockBytes;
+constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
+static_assert(kOffValid + 8 * kValidRing <= kOffFin && kOffMx + 1024 <= kOffK, "header");
+// The key-validity masks travel through their own ring of kValidRing
+// barriers: the producers fill a tile only after the QK products have read
+// part of the tile two back, and those products wait for the softmax of the
+// tile two before that, so the producers run at most five tiles ahead of the
+// softmax warps and a parity wait on this ring is never two phases behind.
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;      // QK CTA: Q, 288 columns
@@ -142,44 +164,57 @@ __device__ __forceinline__ int checked_row(const Params& p, int raw) {
   return (raw >= 0 && int64_t(raw) < p.num_slots) ? raw : -1;
 }
 
-// Producer warps (224 threads): bring each 64-key tile into the stage ring in
-// the 128B-swizzled K-major layout (column block c/8, row `key`, 16-byte
-// chunk (c%8) ^ (key%8)).
-//  - Paged keys, or a split's ragged last tile: 16-byte cp.async copies from
-//    every producer thread (zero-filled for keys without a row).  The tile's
-//    pool rows are staged in shared memory and fetched one tile ahead.
+// Producer warps (224 threads): bring each 64-key tile into its ring slots in
+// the 128B-swizzled K-major layout (column block c -> slot (nb*t + c) mod
+// kRing; inside a slot row `key`, 16-byte chunk (c%8) ^ (key%8)).
+//  - Paged keys, or a split's ragged last tile: 16-byte cp.async copies, one
+//    warp per key (lane l copies chunks l, l+32, l+64, so one warp instruction
+//    moves 512 contiguous bytes of the row), zero-filled for keys without a
+//    row.  The tile's pool rows are staged in shared memory and fetched one
+//    tile ahead.
 //  - Contiguous keys (kv_start) for a whole in-range tile: TMA tiled box
-//    loads.  With a 3-D map (column-in-block, pool row, column block) one box
-//    of 64 columns x 64 rows x all column blocks lands the whole tile in the
-//    staged layout with a single instruction; otherwise one 64 x 64 box per
-//    column block.
-// With kMask the tile's 64-bit key-validity mask goes to the ring read by the
-// softmax warps.  Completion: every producer's cp.async arrival (noinc) plus
-// one arrival of producer 0 (with the TMA byte count when boxes are used,
-// after the mask is written).  Returns false when a bounded wait gave up (all
-// producers agree through the named barrier).
-template <int kChunks, int kStages, bool kMask>
+//    loads.  When the tile's slots do not wrap around the ring, one 3-D box
+//    (64 columns x 64 rows x nb column blocks, map `map3`) lands the whole
+//    tile; otherwise one 64 x 64 box per column block (2-D map `map2`).
+// Before filling a tile, producer 0 waits for the release of its slots by the
+// products of the tiles that used them before.  With kMask the
+// tile's 64-bit key-validity mask goes to the ring read by the softmax warps.
+// Completion: every producer's cp.async arrival (noinc) on the tile's full
+// barrier plus one arrival of producer 0 (carrying the TMA byte count when
+// boxes are used).  Returns false when a bounded wait gave up (all producers
+// agree through the named barrier).
+template <int kBlocks, int kRing, bool kMask>
 __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, const SplitRange& sr,
-                                        int ntiles, int ptid, uint32_t stage_base,
-                                        uint32_t stage_bytes, uint32_t full0, uint32_t empty0,
-                                        int* srow, uint32_t* valid32, uint32_t vready0,
-                                        volatile int* abort_flag, const CUtensorMap* tmap,
+                                        int ntiles, int ptid, uint32_t ring, uint32_t full0,
+                                        uint32_t empty0, int* srow, uint32_t* valid32,
+                                        uint32_t vready0, volatile int* abort_flag,
+                                        const CUtensorMap* map3, const CUtensorMap* map2,
                                         bool box3d) {
+  constexpr int kChunks = kBlocks * 8;
   const int lane = ptid & 31;
   int raw = ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
-    const int s = t % kStages;
+    const int g0 = kBlocks * t;   // ring position of the tile's first block
+    const int s0 = g0 % kRing;
     bool got = true;
-    // one thread polls the stage's release; the others learn the outcome at
-    // the named barrier below
-    if (t >= kStages && ptid == 0)
-      got = mbar_wait(empty0 + 8u * uint32_t(s), uint32_t((t / kStages) - 1) & 1u, abort_flag,
-                      kWaitCycles);
+    // Producer 0 waits for the release of the slot of the tile's last block
+    // only: its previous occupant is the latest of the previous occupants in
+    // issue order, and a commit arrives only once every earlier product has
+    // completed, so all of the tile's slots are free then.  (One blocking wait
+    // per tile: each one costs a wake-up latency, and nine in a row cost more
+    // than the deeper ring gains.)  The others learn the outcome at the named
+    // barrier below.
+    {
+      const int g = g0 + kBlocks - 1;
+      if (ptid == 0 && g >= kRing)
+        got = mbar_wait(empty0 + 8u * uint32_t(g % kRing), uint32_t(g / kRing - 1) & 1u, abort_flag,
+                        kWaitCycles);
+    }
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
     if (ptid < 64) {
       const int rw = checked_row(p, raw);
-      srow[s * 64 + ptid] = rw;
+      srow[(t & 1) * 64 + ptid] = rw;
       if (kMask) {
         const int j = sr.k0 + t * kTile + ptid;
         if (j < sr.k1 && rw < 0) atomicOr(p.status, VA_STATUS_BAD_SLOT);
@@ -191,7 +226,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
       ok = false;
       break;
     }
-    const uint32_t dst0 = stage_base + uint32_t(s) * stage_bytes;
+    const uint32_t fb = full0 + 8u * uint32_t(t & 1);
     // contiguous rows, whole tile inside the split and the pool: box loads
     const int tk0 = sr.k0 + t * kTile;
     const int64_t row0 = p.kv_start ? ri.base + tk0 : -1;
@@ -200,40 +235,46 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     if (kMask && ptid == 0) mbar_arrive(vready0 + 8u * uint32_t(t % kValidRing));
     if (ptid == 0) {
       if (boxes) {
-        mbar_arrive_expect_tx(full0 + 8u * uint32_t(s), uint32_t(kChunks / 8) * kBlockBytes);
-        if (box3d) {
-          tma_load_3d(dst0, tmap, 0, int(row0), 0, full0 + 8u * uint32_t(s));
+        mbar_arrive_expect_tx(fb, uint32_t(kBlocks) * kBlockBytes);
+        if (box3d && s0 + kBlocks <= kRing) {
+          tma_load_3d(ring + uint32_t(s0) * kBlockBytes, map3, 0, int(row0), 0, fb);
         } else {
 #pragma unroll 1
-          for (int c = 0; c < kChunks / 8; ++c)
-            tma_load_2d(dst0 + uint32_t(c) * kBlockBytes, tmap, 64 * c, int(row0),
-                        full0 + 8u * uint32_t(s));
+          for (int c = 0; c < kBlocks; ++c) {
+            const int sl = s0 + c < kRing ? s0 + c : s0 + c - kRing;
+            tma_load_2d(ring + uint32_t(sl) * kBlockBytes, map2, 64 * c, int(row0), fb);
+          }
         }
       } else {
-        mbar_arrive(full0 + 8u * uint32_t(s));
+        mbar_arrive(fb);
       }
     }
     if (ptid < 64 && t + 1 < ntiles) raw = fetch_row(p, ri, sr.k0 + (t + 1) * kTile + ptid, sr.k1);
     if (!boxes) {
-      // warp per key: lane l copies 16-byte chunks l, l+32, l+64 of the row,
-      // so one warp instruction moves 512 contiguous bytes
+      // this lane's chunks lane + 32j lie in column blocks lane/8 + 4j, at
+      // chunk position lane%8 inside their 128-byte row
+      uint32_t slot_addr[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int cb = (lane >> 3) + 4 * j;
+        const int sl = s0 + cb < kRing ? s0 + cb : s0 + cb - kRing;
+        slot_addr[j] = ring + uint32_t(sl) * kBlockBytes;
+      }
       const int pw = ptid >> 5;
 #pragma unroll 2
       for (int key = pw; key < kTile; key += kProducers / 32) {
-        const int row = srow[s * 64 + key];
+        const int row = srow[(t & 1) * 64 + key];
         const __nv_bfloat16* src = p.kv + (row >= 0 ? int64_t(row) * p.kv_stride : 0);
         const uint32_t nb = row >= 0 ? 16u : 0u;
-        const uint32_t kd = dst0 + uint32_t(key) * 128u;
+        const uint32_t kx = uint32_t(key) * 128u + uint32_t(((lane & 7) ^ (key & 7)) * 16);
 #pragma unroll
-        for (int j = 0; j < (kChunks + 31) / 32; ++j) {
+        for (int j = 0; j < 3; ++j) {
           const int c = lane + 32 * j;
-          if (c < kChunks)
-            cp_async16(kd + uint32_t(c >> 3) * kBlockBytes + uint32_t(((c & 7) ^ (key & 7)) * 16),
-                       src + c * 8, nb);
+          if (c < kChunks) cp_async16(slot_addr[j] + kx, src + c * 8, nb);
         }
       }
     }
-    cp_async_arrive_noinc(full0 + 8u * uint32_t(s));
+    cp_async_arrive_noinc(fb);
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
   }
   cp_async_wait_all();
@@ -276,7 +317,8 @@ __device__ __forceinline__ void load_q(const Params& p, int b, int row0, int hal
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, int box3d) {
+                      const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ CUtensorMap tmap_2d, int box3d) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -305,8 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_OCORR || i == B_QREADY) cnt = kSoftmax;
-      if (i >= B_KFULL && i < B_KFULL + kKStages) cnt = kProducers + 1;   // copies + producer 0
-      if (i >= B_VFULL && i < B_VFULL + kVStages) cnt = kProducers + 1;
+      if (i == B_FULL || i == B_FULL + 1) cnt = kProducers + 1;   // copies + producer 0
       if (i == B_FIN) cnt = 4;   // one per warp of the first softmax warpgroup
       mbar_init(bar(i), cnt);
     }
@@ -314,7 +355,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) tmem_alloc(sb + kOffTmemSlot, kTmemCols);
-  if (tid == 0 && p.kv_start) tma_prefetch(rank == 0 ? &tmap_k : &tmap_v);
+  if (tid == 0 && p.kv_start) {
+    tma_prefetch(rank == 0 ? &tmap_k : &tmap_v);
+    tma_prefetch(&tmap_2d);
+  }
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
@@ -329,10 +373,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile uint64_t* valid_ring = reinterpret_cast<volatile uint64_t*>(gb + kOffValid);
     if (producer) {
       // ---- producers: K tiles (all 576 columns)
-      if (!produce<kDqk / 8, kKStages, true>(p, ri, sr, ntiles, ptid, sb + kOffK, kKStageBytes,
-                                             bar(B_KFULL), bar(B_KEMPTY), srow,
-                                             reinterpret_cast<uint32_t*>(gb + kOffValid),
-                                             bar(B_VREADY), abort_flag, &tmap_k, box3d != 0) &&
+      if (!produce<kKBlocks, kRingK, true>(p, ri, sr, ntiles, ptid, sb + kOffK, bar(B_FULL),
+                                           bar(B_EMPTY), srow,
+                                           reinterpret_cast<uint32_t*>(gb + kOffValid),
+                                           bar(B_VREADY), abort_flag, &tmap_k, &tmap_2d,
+                                           box3d != 0) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
@@ -343,9 +388,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) fail();
       constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % kKStages, bs = t & 1;
+        const int bs = t & 1;
         const bool got =
-            mbar_wait(bar(B_KFULL + s), uint32_t(t / kKStages) & 1u, abort_flag, kWaitCycles) &&
+            mbar_wait(bar(B_FULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
             (t < 2 || mbar_wait(bar(B_SEMPTY + bs), uint32_t((t >> 1) - 1) & 1u, abort_flag,
                                 kWaitCycles));
         if (!__all_sync(0xffffffffu, got)) {
@@ -355,18 +400,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_cta();   // the producers' cp.async writes, seen by the tensor core
         tc_fence_after();
         if (lane == 0) VA_TRACE_EVENT(1, 0, t);
-        const uint64_t bd0 =
-            smem_desc(sb + kOffK + uint32_t(s) * kKStageBytes, 16, 1024, kSwizzle128B);
+        const int s0 = (kKBlocks * t) % kRingK;
         const uint32_t d = tmem + kTmemS + 64u * uint32_t(bs);
-        // K columns 16k..16k+15: column block k/4, 32-byte step k%4 inside the
-        // swizzled row (the descriptor's address field counts 16-byte units)
+        // K columns 16k..16k+15 (k = 4c + kk): column block c in its ring
+        // slot, 32-byte step kk inside the swizzled row (the descriptor's
+        // address field counts 16-byte units); each slot is released as soon
+        // as its four products complete
 #pragma unroll
-        for (int k = 0; k < kDqk / 16; ++k)
-          mma_ts_warp(d, tmem + kTmemQ + 8u * uint32_t(k),
-                      bd0 + uint64_t((uint32_t(k >> 2) * kBlockBytes + uint32_t(k & 3) * 32u) >> 4),
-                      idesc, k > 0 ? 1u : 0u);
+        for (int c = 0; c < kKBlocks; ++c) {
+          const int sl = s0 + c < kRingK ? s0 + c : s0 + c - kRingK;
+          const uint64_t bd =
+              smem_desc(sb + kOffK + uint32_t(sl) * kBlockBytes, 16, 1024, kSwizzle128B);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_warp(d, tmem + kTmemQ + 8u * uint32_t(4 * c + kk),
+                        bd + uint64_t((uint32_t(kk) * 32u) >> 4), idesc, (c | kk) != 0 ? 1u : 0u);
+          mma_commit_warp(bar(B_EMPTY + sl));
+        }
         mma_commit_warp(bar(B_SFULL + bs));
-        mma_commit_warp(bar(B_KEMPTY + s));
         if (lane == 0) VA_TRACE_EVENT(1, 1, t);
       }
       mma_commit_warp(bar(B_MMAFIN));
@@ -510,14 +561,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile uint32_t* cmd = reinterpret_cast<volatile uint32_t*>(gb + kOffCmd);
     if (producer) {
       // ---- producers: value columns of the same tiles
-      if (!produce<kDv / 8, kVStages, false>(p, ri, sr, ntiles, ptid, sb + kOffV, kVStageBytes,
-                                             bar(B_VFULL), bar(B_VEMPTY), srow, nullptr, 0u,
-                                             abort_flag, &tmap_v, box3d != 0) &&
+      if (!produce<kVBlocks, kRingV, false>(p, ri, sr, ntiles, ptid, sb + kOffV, bar(B_FULL),
+                                            bar(B_EMPTY), srow, nullptr, 0u, abort_flag, &tmap_v,
+                                            &tmap_2d, box3d != 0) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
       // ---- MMA issuer: O += P_t V_t (whole warp, one elected lane issues)
-      constexpr uint32_t idesc = idesc_bf16(128, 256, 0, 1);
+      constexpr uint32_t idesc = idesc_bf16(128, 64 * kVGroup, 0, 1);
       uint32_t nresc = 0;
       // each P buffer's barrier expects one arrival (ours, carrying the byte
       // count of the QK CTA's bulk copy into it): arm the first uses now
@@ -526,9 +577,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(B_PFULL + t), kPPayload);
       __syncwarp();
       for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kVStages, bs = t % kPBufs;
+        const int bs = t % kPBufs;
         const bool got =
-            mbar_wait(bar(B_VFULL + s), uint32_t(t / kVStages) & 1u, abort_flag, kWaitCycles) &&
+            mbar_wait(bar(B_FULL + (t & 1)), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
             mbar_wait<true>(bar(B_PFULL + bs), uint32_t(t / kPBufs) & 1u, abort_flag, kWaitCycles);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) fail();
@@ -565,24 +616,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_cta();
         tc_fence_after();
         const uint64_t ad0 = smem_desc(pbase, 16, 1024, kSwizzle128B);
-        const uint64_t bd0 =
-            smem_desc(sb + kOffV + uint32_t(s) * kVStageBytes, kBlockBytes, 1024, kSwizzle128B);
-        // O columns [256h, 256h+256) += P keys 16k..16k+15 x V rows of those
-        // keys: A steps 32 bytes inside P's swizzled rows, B steps two 8-key
-        // groups (2 KB) down the value tile, whose column blocks 4h..4h+3
-        // form the 256-wide N extent (8 KB apart)
+        const int s0 = (kVBlocks * t) % kRingV;
+        // O columns [256q, 256q+256) += P keys 16k..16k+15 x V rows of those
+        // keys: A steps 32 bytes inside P's swizzled rows; B is the value
+        // column blocks 4q..4q+3 (adjacent ring slots, 8 KB apart: the N
+        // extent) and steps two 8-key groups (2 KB) down them.  The group's
+        // slots are released once its four products complete.
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int q = 0; q < kVBlocks / kVGroup; ++q) {
+          const int sl = s0 + kVGroup * q < kRingV ? s0 + kVGroup * q : s0 + kVGroup * q - kRingV;
+          const uint64_t bd =
+              smem_desc(sb + kOffV + uint32_t(sl) * kBlockBytes, kBlockBytes, 1024, kSwizzle128B);
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_ss_warp(tmem + 256u * uint32_t(h), ad0 + uint64_t((uint32_t(k) * 32u) >> 4),
-                        bd0 + uint64_t((uint32_t(4 * h) * kBlockBytes + uint32_t(k) * 2048u) >> 4),
-                        idesc, (t > 0 || k > 0) ? 1u : 0u);
+            mma_ss_warp(tmem + uint32_t(64 * kVGroup * q), ad0 + uint64_t((uint32_t(k) * 32u) >> 4),
+                        bd + uint64_t((uint32_t(k) * 2048u) >> 4), idesc,
+                        (t > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+          for (int b = 0; b < kVGroup; ++b) mma_commit_warp(bar(B_EMPTY + sl + b));
+        }
         // re-arm the buffer for tile t + kPBufs before its release reaches
         // the QK CTA (the release follows this product's completion)
         if (lane == 0 && t + kPBufs < ntiles) mbar_arrive_expect_tx(bar(B_PFULL + bs), kPPayload);
         __syncwarp();
-        mma_commit_warp(bar(B_VEMPTY + s));
         mma_commit_mc_warp(bar(B_PFREE + bs), uint16_t(1u << 0));
         if (lane == 0) VA_TRACE_EVENT(4, 1, t);
       }
@@ -723,21 +779,17 @@ bool encode_pool_map(CUtensorMap* m, const Params& p, int blocks) {
 cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
   // Contiguous pools are read with TMA box loads; the maps are encoded on the
   // host for this call's pool.  Paged calls do not use them.
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, t2;
   memset(&tk, 0, sizeof tk);
   memset(&tv, 0, sizeof tv);
+  memset(&t2, 0, sizeof t2);
   int box3d = 0;
   if (p.kv_start) {
-    if (!g_encode) return cudaErrorNotSupported;
-    if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) {
-      box3d = 1;
-    } else {
-      if (!encode_pool_map(&tk, p, 0)) return cudaErrorNotSupported;
-      tv = tk;
-    }
+    if (!g_encode || !encode_pool_map(&t2, p, 0)) return cudaErrorNotSupported;
+    if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) box3d = 1;
   }
   dim3 grid(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
-  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv, box3d);
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv, t2, box3d);
   return cudaGetLastError();
 }
 
