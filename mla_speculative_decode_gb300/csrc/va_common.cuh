@@ -158,8 +158,18 @@ __device__ inline uint32_t smem_u32(const void* ptr) {
       g_va_trace[((role) * 8 + (ev)) * 512 + (t)] = _ts;                                  \
     }                                                                                    \
   } while (0)
+// Per-cluster marks of the partial kernel: slot (role, ev, cluster index).
+#define VA_TRACE_CTA(role, ev)                                                             \
+  do {                                                                                     \
+    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && (blockIdx.x >> 1) < 512) {       \
+      unsigned long long _ts;                                                               \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                                \
+      g_va_trace[((role) * 8 + (ev)) * 512 + (blockIdx.x >> 1)] = _ts;                      \
+    }                                                                                      \
+  } while (0)
 #else
 #define VA_TRACE_EVENT(role, ev, t) ((void)0)
+#define VA_TRACE_CTA(role, ev) ((void)0)
 #endif
 
 // Launchers (defined in the kernel translation units).

@@ -14,9 +14,9 @@
 
 namespace va {
 cudaError_t init_partial_fma();
-cudaError_t init_partial_tc();
+cudaError_t init_partial_tc(int* max_pairs);
 bool tc_supported(int B, int T, int H);
-int tc_auto_nsplit(int B, int T, int H, int num_sms);
+int tc_auto_nsplit(int B, int T, int H, int pairs);
 cudaError_t launch_partial_tc(const Params& p, int num_sms, cudaStream_t st);
 }  // namespace va
 
@@ -26,6 +26,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   int ready;
   int num_sms;
+  int tc_pairs;   // two-CTA clusters of the tensor-core kernel resident at once
 };
 DeviceState g_dev[kMaxDevices];   // written by va_init only
 cudaEvent_t g_ev_before = nullptr; // benchmark timing hook (va_set_partial_events)
@@ -99,7 +100,7 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   if (path < 0) return VA_ERR_UNSUPPORTED;
   int ns = nsplit;
   if (ns == 0)
-    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.num_sms)
+    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
                             : auto_nsplit_fma(B, T, H, ds.num_sms);
   const va::WsLayout L = va::ws_layout(B, T, H, ns);
   if (ws_bytes < L.total) return VA_ERR_WORKSPACE;
@@ -162,10 +163,12 @@ VA_API int va_init(int device) {
   if (cudaGetDevice(&prev) != cudaSuccess) return VA_ERR_CUDA;
   if (cudaSetDevice(device) != cudaSuccess) return VA_ERR_CUDA;
   cudaError_t e1 = va::init_partial_fma();
-  cudaError_t e2 = va::init_partial_tc();
+  int pairs = 0;
+  cudaError_t e2 = va::init_partial_tc(&pairs);
   cudaSetDevice(prev);
   if (e1 != cudaSuccess || e2 != cudaSuccess) return VA_ERR_CUDA;
   g_dev[device].num_sms = prop.multiProcessorCount;
+  g_dev[device].tc_pairs = pairs > 0 ? pairs : prop.multiProcessorCount / 2;
   g_dev[device].ready = 1;
   return VA_OK;
 }
@@ -178,7 +181,7 @@ VA_API int va_auto_nsplit(int B, int T, int H, int flags) {
   if (rc != VA_OK) return rc;
   const int path = pick_path(flags, B, T, H);
   if (path < 0) return VA_ERR_UNSUPPORTED;
-  return path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.num_sms)
+  return path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
                             : auto_nsplit_fma(B, T, H, ds.num_sms);
 }
 
@@ -260,7 +263,7 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
   if (ns == 0) {
     const int path = pick_path(flags, B, T, H);
     if (path < 0) return VA_ERR_UNSUPPORTED;
-    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.num_sms)
+    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
                             : auto_nsplit_fma(B, T, H, ds.num_sms);
     while (ns > 1 && va::ws_layout(B, T, H, ns).total > cap) --ns;
   }

@@ -118,9 +118,14 @@ constexpr uint32_t kOffStage = kOffK + kRingK * kBlockBytes;   // QK: P staging 
 constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
 constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V ring
 constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
+// PV epilogue staging: 64 rows of 2 KB + 16 bytes (the pad spreads rows over
+// the banks) at kOffP, over the P and value buffers
+constexpr uint32_t kEpiRowBytes = 2048 + 16;
 constexpr uint32_t kEndPV = kOffV + kRingV * kBlockBytes;
 constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffP + 64 * kEpiRowBytes <= kEndPV, "epilogue staging");
+static_assert(8 * 4096 <= 2 * kPBufBytes, "Q load scratch in the P staging buffers");
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
 static_assert(kOffValid + 8 * kValidRing <= kOffFin && kOffMx + 1024 <= kOffK, "header");
 // The key-validity masks travel through their own ring of kValidRing
@@ -282,32 +287,49 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
 }
 
 // Q rows into TMEM as the A operand (bf16 pairs, 288 columns).  The two
-// softmax warpgroups share the work: warp w writes lane quadrant w%4, column
-// chunks 0-4 (first warpgroup) or 5-8 (second) of 32 columns (64 features
-// each), at most 3 chunks per round trip to memory.
+// softmax warpgroups share the work: warp w writes lane quadrant w%4 (rows
+// 32*(w%4) .. +31) for column chunks 0-4 (first warpgroup) or 5-8 (second),
+// 64 features (128 bytes) per chunk.  Global reads are coalesced -- one warp
+// instruction reads 128 contiguous bytes of each of four rows -- and go
+// through the warp's own 4 KB of shared scratch (`scratch`, 128B-swizzled
+// rows) so that lane r then holds row r's chunk for tcgen05.st.  Two chunks
+// are in flight per round trip to memory.
 __device__ __forceinline__ void load_q(const Params& p, int b, int row0, int half, int q4, int lane,
-                                       uint32_t tmem) {
-  const int lr = row0 + q4 * 32 + lane;
-  const bool ok = lr < p.rows_per_req;
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t(b) * p.rows_per_req + lr) * kDqk);
-  const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + kTmemQ;
+                                       uint32_t tmem, uint8_t* scratch) {
   const int c_begin = half ? 5 : 0, c_end = half ? 9 : 5;
+  const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + kTmemQ;
+  const int sub = lane >> 3, piece = lane & 7;   // row within a group of 4, 16-byte piece
 #pragma unroll 1
-  for (int c0 = c_begin; c0 < c_end; c0 += 3) {
-    const int n = c_end - c0 < 3 ? c_end - c0 : 3;
-    uint4 buf[24];
+  for (int c0 = c_begin; c0 < c_end; c0 += 2) {
+    const int n = c_end - c0 < 2 ? c_end - c0 : 2;
+    uint4 buf[2][8];
 #pragma unroll
-    for (int i = 0; i < 24; ++i)
-      buf[i] = (ok && i < 8 * n) ? src[c0 * 8 + i] : make_uint4(0, 0, 0, 0);
+    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-    for (int cc = 0; cc < 3; ++cc) {
+      for (int i = 0; i < 8; ++i) {
+        const int lr = row0 + q4 * 32 + 4 * i + sub;
+        buf[cc][i] = (cc < n && lr < p.rows_per_req)
+                         ? *reinterpret_cast<const uint4*>(
+                               p.q + (size_t(b) * p.rows_per_req + lr) * kDqk + (c0 + cc) * 64 +
+                               piece * 8)
+                         : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
       if (cc < n) {
-        uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          v[4 * i] = buf[cc * 8 + i].x; v[4 * i + 1] = buf[cc * 8 + i].y;
-          v[4 * i + 2] = buf[cc * 8 + i].z; v[4 * i + 3] = buf[cc * 8 + i].w;
+          const int rr = 4 * i + sub;
+          *reinterpret_cast<uint4*>(scratch + rr * 128 + ((piece ^ (rr & 7)) * 16)) = buf[cc][i];
         }
+        __syncwarp();
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(scratch + lane * 128 + ((j ^ (lane & 7)) * 16));
+          v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+        }
+        __syncwarp();
         tmem_st32(tl + 32u * uint32_t(c0 + cc), v);
       }
     }
@@ -329,6 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int split = blockIdx.x >> 1, rb = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 0);
 
   const ReqInfo ri = req_info(p, b, split == 0 && rb == 0 && rank == 0 && tid == 0);
   const SplitRange sr = split_range(ri.N, p.nsplit, split);
@@ -362,6 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
+  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 1);
   const bool producer = warp == 0 || warp == 2 || warp == 3 || warp >= 12;
   const int ptid = warp == 0 ? lane : (warp < 4 ? warp - 1 : warp - 9) * 32 + lane;
   int* srow = reinterpret_cast<int*>(gb + kOffSrow);
@@ -426,9 +450,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
       // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of
       // every tile for row r
-      load_q(p, b, row0, half, q4, lane, tmem);
+      // the P staging buffers are free until the first tile: 4 KB of Q
+      // transposition scratch per softmax warp
+      load_q(p, b, row0, half, q4, lane, tmem, gb + kOffStage + uint32_t(warp - 4) * 4096u);
       tc_fence_before();
       mbar_arrive(bar(B_QREADY));
+      if (tid == 128) VA_TRACE_CTA(6, 5);
       const int r = q4 * 32 + lane;
       const int lr = row0 + r;
       const bool row_ok = lr < R;
@@ -689,46 +716,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const bool fin = ok && mbar_wait<true>(bar(B_FIN), 0, abort_flag, kWaitCycles) &&
                        mbar_wait(bar(B_MMAFIN), 0, abort_flag, kWaitCycles);
-      if (__all_sync(0xffffffffu, fin)) {
+      // all row warps agree before the staged write-out below
+      const bool go = named_sync_and(kSoftmaxBar, kSoftmax, __all_sync(0xffffffffu, fin));
+      if (go) {
+        if (tid == 128) VA_TRACE_CTA(7, 5);
         tc_fence_after();
+        // The split's partial (128 rows x 512 fp32, normalised by the row
+        // sum) leaves through shared memory so that every warp store writes
+        // 512 contiguous bytes of a row: the P and value buffers are idle now
+        // and hold 64 padded rows per pass.
         const float inv = reinterpret_cast<const float*>(gb + kOffFin)[r];
-        float* dst = p.part_o + (size_t(split) * rows_total + size_t(b) * R + lr) * kDv + 256 * half;
+        uint8_t* stg = gb + kOffP;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + 32u * uint32_t(c), v);
-          tmem_wait_ld();
-          if (row_ok) {
+        for (int pass = 0; pass < 2; ++pass) {
+          if ((q4 >> 1) == pass) {
+            uint8_t* rowp = stg + (r - 64 * pass) * kEpiRowBytes + 1024 * half;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tl + 32u * uint32_t(c), v);
+              tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + 32 * c + e) =
-                  make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                              __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(rowp + (32 * c + e) * 4) =
+                    make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
+                                __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+            }
           }
+          named_sync(kSoftmaxBar, kSoftmax);
+          // 64 rows x 2 KB as 256 segments of 512 bytes, one per warp store
+#pragma unroll 4
+          for (int sg = warp - 4; sg < 256; sg += kSoftmax / 32) {
+            const int rr = sg >> 2, part = sg & 3;
+            const int lrr = row0 + 64 * pass + rr;
+            if (lrr < R) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * kEpiRowBytes + part * 512 +
+                                                              lane * 16);
+              *reinterpret_cast<uint4*>(p.part_o +
+                                        (size_t(split) * rows_total + size_t(b) * R + lrr) * kDv +
+                                        part * 128 + lane * 4) = w;
+            }
+          }
+          named_sync(kSoftmaxBar, kSoftmax);
         }
-      } else if (ok) {
+      } else if (ok && !fin) {
         fail();
       }
     }
   }
 
+  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 2);
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 3);
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
   cluster_sync();
+  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 4);
 }
 
 }  // namespace
 
 bool tc_supported(int, int, int) { return true; }
 
-int tc_auto_nsplit(int B, int T, int H, int num_sms) {
+// Splits per (row block, request) so that all clusters are co-resident:
+// `pairs` is the number of two-CTA clusters the device runs at once (clusters
+// live inside one GPC, so GPCs with an odd SM count strand an SM, and a grid
+// of num_sms / 2 clusters would leave a second, nearly empty wave).
+int tc_auto_nsplit(int B, int T, int H, int pairs) {
   const long rowblocks = (long(T) * H + kRows - 1) / kRows;
   const long items = rowblocks * B;
-  const long pairs = num_sms / 2;
   long ns = pairs / items;
   if (ns < 1) ns = 1;
   if (ns > VA_NSPLIT_MAX) ns = VA_NSPLIT_MAX;
@@ -737,10 +796,21 @@ int tc_auto_nsplit(int B, int T, int H, int num_sms) {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-cudaError_t init_partial_tc() {
+cudaError_t init_partial_tc(int* max_pairs) {
   cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemBytes));
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, partial_tc_kernel, &cfg) != cudaSuccess) {
+    n = 0;
+    (void)cudaGetLastError();
+  }
+  *max_pairs = n;
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
