@@ -13,6 +13,7 @@
 // each request's KV contiguous).  A warp copies whole rows with 16-byte
 // loads and stores; every source and destination row is range-checked.
 #include <math.h>
+#include <string.h>
 
 #include "va_common.cuh"
 
@@ -39,21 +40,41 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
   return r;
 }
 
-// Grid (row, 128-column chunk).  The split weights exp(lse_s - lse) are formed
-// once per CTA in shared memory; each warp then sums its share of the splits
-// for the chunk (a float4 per lane) and the eight partial sums are added.
+// Grid (row, 128-column chunk).  Each warp first issues the loads of its
+// share of the splits' partial outputs for the chunk (a float4 per lane, up to
+// kBuf splits per warp in flight) -- they do not depend on the weights, so
+// their round trip to memory overlaps the one of the lse values.  The split
+// weights exp(lse_s - lse) are formed once per CTA in shared memory; each warp
+// then sums its splits and the eight partial sums are added.  Loads of splits
+// past the request's effective split count (slots the split-K kernel did not
+// write) are never used: their terms are selected out, not multiplied by 0.
+constexpr int kBuf = 10;   // splits per warp per round (80 per CTA)
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   __shared__ float wsplit[kMaxSplits];
   __shared__ float red[kCombineThreads / 32];
   __shared__ float4 part[kCombineThreads / 32][kCombineCols / 4];
+  griddep_wait();   // the split-K kernel's partials are complete and visible
   const int rows_total = p.B * p.rows_per_req;
   const int row = blockIdx.x, chunk = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = row / p.rows_per_req;
+  constexpr int kWarps = kCombineThreads / 32;
+  const float* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
+  const size_t sstride = size_t(rows_total) * kDv;
+
+  // first round of partial-output loads (splits warp, warp + 8, ...)
+  float4 buf[kBuf];
+#pragma unroll
+  for (int i = 0; i < kBuf; ++i) {
+    const int s = warp + kWarps * i;
+    buf[i] = s < p.nsplit ? *reinterpret_cast<const float4*>(po + size_t(s) * sstride)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
   const ReqInfo ri = req_info(p, b, false);
   const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
   const float* pl = p.part_lse + row;
-
   float m = -INFINITY;
   for (int s = tid; s < ne; s += kCombineThreads) {
     const float ls = pl[size_t(s) * rows_total];
@@ -72,23 +93,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   __syncthreads();
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
-  const size_t sstride = size_t(rows_total) * kDv;
-#pragma unroll 4
-  for (int s = warp; s < ne; s += kCombineThreads / 32) {
-    const float w = wsplit[s];
-    const float4 o = *reinterpret_cast<const float4*>(po + size_t(s) * sstride);
-    acc.x = fmaf(w, o.x, acc.x);
-    acc.y = fmaf(w, o.y, acc.y);
-    acc.z = fmaf(w, o.z, acc.z);
-    acc.w = fmaf(w, o.w, acc.w);
+  for (int base = 0; base < ne; base += kWarps * kBuf) {
+    if (base > 0) {
+#pragma unroll
+      for (int i = 0; i < kBuf; ++i) {
+        const int s = base + warp + kWarps * i;
+        buf[i] = s < ne ? *reinterpret_cast<const float4*>(po + size_t(s) * sstride)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBuf; ++i) {
+      const int s = base + warp + kWarps * i;
+      if (s < ne) {
+        const float w = wsplit[s];
+        acc.x = fmaf(w, buf[i].x, acc.x);
+        acc.y = fmaf(w, buf[i].y, acc.y);
+        acc.z = fmaf(w, buf[i].z, acc.z);
+        acc.w = fmaf(w, buf[i].w, acc.w);
+      }
+    }
   }
   part[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
     float4 t = part[0][lane];
 #pragma unroll
-    for (int w = 1; w < kCombineThreads / 32; ++w) {
+    for (int w = 1; w < kWarps; ++w) {
       const float4 u = part[w][lane];
       t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
     }
@@ -138,8 +169,20 @@ __global__ void __launch_bounds__(kDefragThreads)
 cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   const int rows_total = p.B * p.rows_per_req;
   dim3 grid(unsigned(rows_total), unsigned(kDv / kCombineCols), 1u);
-  combine_kernel<<<grid, kCombineThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  // launched with programmatic stream serialization: its blocks may be
+  // scheduled as the split-K kernel's clusters retire and wait in-kernel
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 cudaError_t launch_defrag(void* pool, int64_t num_slots, int64_t stride, const int32_t* src,

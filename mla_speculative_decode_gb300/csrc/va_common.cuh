@@ -149,6 +149,17 @@ __device__ inline uint32_t smem_u32(const void* ptr) {
 // defined; a traced build records %globaltimer per (role, event, tile) for the
 // first cluster of the grid into the device buffer `g_va_trace`, which the
 // translation unit that uses the macro defines.
+// Programmatic dependent launch.  The kernels of a step run back to back on
+// one stream; a kernel launched with programmatic stream serialization may
+// start while its predecessor still runs, and griddep_wait() holds the calling
+// thread until the predecessor has completed and its writes are visible (for a
+// kernel launched the ordinary way it returns at once).  A kernel calls
+// griddep_launch_dependents() to let its successor start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 #ifdef VA_TRACE
 #define VA_TRACE_EVENT(role, ev, t)                                                        \
   do {                                                                                   \

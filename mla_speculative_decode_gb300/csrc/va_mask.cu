@@ -22,6 +22,7 @@ constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) tree_bits_kernel(Params p, uint64_t* bits_out) {
   __shared__ int par[kWarps][kTmax];
+  griddep_launch_dependents();   // the split-K kernel may start its set-up now
   if (threadIdx.x == 0) *p.status = 0u;
   __syncthreads();
   if (p.tree_parent == nullptr) return;

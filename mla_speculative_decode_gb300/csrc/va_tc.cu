@@ -199,6 +199,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   const int lane = ptid & 31;
   int raw = ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
+  bool bad_slot = false;
   for (int t = 0; t < ntiles; ++t) {
     const int g0 = kBlocks * t;   // ring position of the tile's first block
     const int s0 = g0 % kRing;
@@ -222,7 +223,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
       srow[(t & 1) * 64 + ptid] = rw;
       if (kMask) {
         const int j = sr.k0 + t * kTile + ptid;
-        if (j < sr.k1 && rw < 0) atomicOr(p.status, VA_STATUS_BAD_SLOT);
+        bad_slot |= j < sr.k1 && rw < 0;
         const uint32_t bal = __ballot_sync(0xffffffffu, rw >= 0);
         if (lane == 0) valid32[(t % kValidRing) * 2 + (ptid >> 5)] = bal;
       }
@@ -283,6 +284,10 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
   }
   cp_async_wait_all();
+  if (kMask && bad_slot) {
+    griddep_wait();
+    atomicOr(p.status, VA_STATUS_BAD_SLOT);
+  }
   return ok;
 }
 
@@ -353,7 +358,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 0);
 
-  const ReqInfo ri = req_info(p, b, split == 0 && rb == 0 && rank == 0 && tid == 0);
+  griddep_launch_dependents();   // the merge kernel may be scheduled as clusters retire
+  // The tree-mask kernel before this one clears the status word and writes
+  // the ancestor masks: every status write and every mask read below follows
+  // a griddep_wait(); the set-up, the Q load and the first gathers overlap it.
+  const ReqInfo ri = req_info(p, b, false);
   const SplitRange sr = split_range(ri.N, p.nsplit, split);
   if (split >= sr.nsplit_eff) return;   // both CTAs of the cluster leave together
   const int R = p.rows_per_req;
@@ -363,6 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   auto fail = [&]() {
     *abort_flag = 1;
+    griddep_wait();
     atomicOr(p.status, VA_STATUS_TIMEOUT);
   };
 
@@ -455,6 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       load_q(p, b, row0, half, q4, lane, tmem, gb + kOffStage + uint32_t(warp - 4) * 4096u);
       tc_fence_before();
       mbar_arrive(bar(B_QREADY));
+      griddep_wait();   // ancestor masks written, status cleared
+      if (split == 0 && rb == 0 && tid == 128) (void)req_info(p, b, true);
       if (tid == 128) VA_TRACE_CTA(6, 5);
       const int r = q4 * 32 + lane;
       const int lr = row0 + r;
@@ -858,9 +870,20 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
     if (!g_encode || !encode_pool_map(&t2, p, 0)) return cudaErrorNotSupported;
     if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) box3d = 1;
   }
-  dim3 grid(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
-  partial_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv, t2, box3d);
-  return cudaGetLastError();
+  // launched with programmatic stream serialization: the clusters start
+  // while the tree-mask kernel runs (see griddep_wait in the kernel)
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p, tk, tv, t2, box3d);
 }
 
 }  // namespace va
