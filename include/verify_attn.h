@@ -103,7 +103,8 @@ int va_auto_nsplit(int B, int T, int H, int flags);
  *   [0, 256)        status word (uint32) and reserved header
  *   tree masks      uint64 [B*T]
  *   partial lse     float  [nsplit][B*T*H]
- *   partial out     float  [nsplit][B*T*H][512]
+ *   partial out     bf16   [nsplit][B*T*H][512] (normalised by the split's
+ *                   row sum; merged in fp32)
  * The Commit That Locked In 6x Decode, "Input Knowledge Required" (NSPLIT and
  * partial-reduce: each split writes a partial result that a reduction merges).
  */

@@ -50,6 +50,10 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
 // write) are never used: their terms are selected out, not multiplied by 0.
 constexpr int kBuf = 10;   // splits per warp per round (80 per CTA)
 
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   __shared__ float wsplit[kMaxSplits];
   __shared__ float red[kCombineThreads / 32];
@@ -60,16 +64,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = row / p.rows_per_req;
   constexpr int kWarps = kCombineThreads / 32;
-  const float* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
+  const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
   const size_t sstride = size_t(rows_total) * kDv;
 
   // first round of partial-output loads (splits warp, warp + 8, ...)
-  float4 buf[kBuf];
+  uint2 buf[kBuf];   // four bf16 partial values per lane
 #pragma unroll
   for (int i = 0; i < kBuf; ++i) {
     const int s = warp + kWarps * i;
-    buf[i] = s < p.nsplit ? *reinterpret_cast<const float4*>(po + size_t(s) * sstride)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    buf[i] = s < p.nsplit ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
+                          : make_uint2(0u, 0u);
   }
 
   const ReqInfo ri = req_info(p, b, false);
@@ -98,8 +102,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 #pragma unroll
       for (int i = 0; i < kBuf; ++i) {
         const int s = base + warp + kWarps * i;
-        buf[i] = s < ne ? *reinterpret_cast<const float4*>(po + size_t(s) * sstride)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        buf[i] = s < ne ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
+                        : make_uint2(0u, 0u);
       }
     }
 #pragma unroll
@@ -107,10 +111,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       const int s = base + warp + kWarps * i;
       if (s < ne) {
         const float w = wsplit[s];
-        acc.x = fmaf(w, buf[i].x, acc.x);
-        acc.y = fmaf(w, buf[i].y, acc.y);
-        acc.z = fmaf(w, buf[i].z, acc.z);
-        acc.w = fmaf(w, buf[i].w, acc.w);
+        const float2 lo = bf16x2_to_float2(buf[i].x), hi = bf16x2_to_float2(buf[i].y);
+        acc.x = fmaf(w, lo.x, acc.x);
+        acc.y = fmaf(w, lo.y, acc.y);
+        acc.z = fmaf(w, hi.x, acc.z);
+        acc.w = fmaf(w, hi.y, acc.w);
       }
     }
   }

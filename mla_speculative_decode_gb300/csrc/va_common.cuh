@@ -30,7 +30,7 @@ __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / 
 struct WsLayout {
   size_t bits;   // uint64 [B*T]
   size_t plse;   // float  [nsplit][rows]
-  size_t po;     // float  [nsplit][rows][512]
+  size_t po;     // bf16   [nsplit][rows][512]
   size_t total;
 };
 
@@ -40,7 +40,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int H, int nsplit) {
   L.bits = kHeaderBytes;
   L.plse = L.bits + align256(size_t(B) * T * sizeof(uint64_t));
   L.po = L.plse + align256(size_t(nsplit) * rows * sizeof(float));
-  L.total = L.po + align256(size_t(nsplit) * rows * kDv * sizeof(float));
+  L.total = L.po + align256(size_t(nsplit) * rows * kDv * sizeof(__nv_bfloat16));
   return L;
 }
 
@@ -62,7 +62,7 @@ struct Params {
   float sm_scale;
   float scale_log2;            // sm_scale * log2(e)
   float* part_lse;             // [nsplit][rows]
-  float* part_o;               // [nsplit][rows][512]
+  __nv_bfloat16* part_o;       // [nsplit][rows][512], normalised by the split's row sum
   uint32_t* status;
   __nv_bfloat16* out;          // [rows, 512]
   float* lse;                  // [rows]

@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kThreads) partial_fma_kernel(Params p) {
     if (row0 + r < R) {
       const float l = S.l[r];
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      *reinterpret_cast<float2*>(p.part_o + ((size_t)split * rows_total + grow0 + r) * kDv + d) =
-          make_float2(acc[r][0] * inv, acc[r][1] * inv);
+      *reinterpret_cast<__nv_bfloat162*>(p.part_o + ((size_t)split * rows_total + grow0 + r) * kDv +
+                                         d) = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
     }
   }
   if (tid < kRB && row0 + tid < R) {

@@ -126,7 +126,7 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   p.sm_scale = sm_scale;
   p.scale_log2 = sm_scale * va::kLog2e;
   p.part_lse = reinterpret_cast<float*>(w + L.plse);
-  p.part_o = reinterpret_cast<float*>(w + L.po);
+  p.part_o = reinterpret_cast<__nv_bfloat16*>(w + L.po);
   p.status = reinterpret_cast<uint32_t*>(w);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;

@@ -220,6 +220,20 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from this CTA's shared memory to global memory, in the executing
+// thread's current bulk group.
+__device__ __forceinline__ void bulk_store_global(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+// Wait until at most N of this thread's bulk groups are pending (writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 
 // Tiled 2-D box load of a tensor map (`map` is a __grid_constant__ kernel

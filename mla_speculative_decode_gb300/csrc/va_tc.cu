@@ -118,13 +118,13 @@ constexpr uint32_t kOffStage = kOffK + kRingK * kBlockBytes;   // QK: P staging 
 constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
 constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V ring
 constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
-// PV epilogue staging: 64 rows of 2 KB + 16 bytes (the pad spreads rows over
-// the banks) at kOffP, over the P and value buffers
-constexpr uint32_t kEpiRowBytes = 2048 + 16;
+// PV epilogue staging: 128 rows of 1 KB (512 bf16) + 16 bytes (the pad
+// spreads rows over the banks) at kOffP, over the P and value buffers
+constexpr uint32_t kEpiRowBytes = 1024 + 16;
 constexpr uint32_t kEndPV = kOffV + kRingV * kBlockBytes;
 constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffP + 64 * kEpiRowBytes <= kEndPV, "epilogue staging");
+static_assert(kOffP + 128 * kEpiRowBytes <= kEndPV, "epilogue staging");
 static_assert(8 * 4096 <= 2 * kPBufBytes, "Q load scratch in the P staging buffers");
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
 static_assert(kOffValid + 8 * kValidRing <= kOffFin && kOffMx + 1024 <= kOffK, "header");
@@ -733,44 +733,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (go) {
         if (tid == 128) VA_TRACE_CTA(7, 5);
         tc_fence_after();
-        // The split's partial (128 rows x 512 fp32, normalised by the row
-        // sum) leaves through shared memory so that every warp store writes
-        // 512 contiguous bytes of a row: the P and value buffers are idle now
-        // and hold 64 padded rows per pass.
+        // The split's partial (128 rows x 512, normalised by the row sum,
+        // rounded to bf16) leaves through shared memory and the bulk-copy
+        // engine, one 1 KB row per copy: the P and value buffers are idle now
+        // and hold all 128 padded rows.
         const float inv = reinterpret_cast<const float*>(gb + kOffFin)[r];
         uint8_t* stg = gb + kOffP;
+        uint8_t* rowp = stg + r * kEpiRowBytes + 512 * half;
 #pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-          if ((q4 >> 1) == pass) {
-            uint8_t* rowp = stg + (r - 64 * pass) * kEpiRowBytes + 1024 * half;
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tl + 32u * uint32_t(c), v);
-              tmem_wait_ld();
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + 32u * uint32_t(c), v);
+          tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(rowp + (32 * c + e) * 4) =
-                    make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                                __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-            }
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * e]) * inv,
+                                                           __uint_as_float(v[2 * e + 1]) * inv);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h);
           }
-          named_sync(kSoftmaxBar, kSoftmax);
-          // 64 rows x 2 KB as 256 segments of 512 bytes, one per warp store
-#pragma unroll 4
-          for (int sg = warp - 4; sg < 256; sg += kSoftmax / 32) {
-            const int rr = sg >> 2, part = sg & 3;
-            const int lrr = row0 + 64 * pass + rr;
-            if (lrr < R) {
-              const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * kEpiRowBytes + part * 512 +
-                                                              lane * 16);
-              *reinterpret_cast<uint4*>(p.part_o +
-                                        (size_t(split) * rows_total + size_t(b) * R + lrr) * kDv +
-                                        part * 128 + lane * 4) = w;
-            }
-          }
-          named_sync(kSoftmaxBar, kSoftmax);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(rowp + 64 * c + 16 * j) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
+        fence_proxy_async_cta();   // staged rows, read by the bulk copies
+        if (tid == 128) VA_TRACE_CTA(5, 0);
+        named_sync(kSoftmaxBar, kSoftmax);
+        // warps 4-7 issue the row copies, one row per lane, and wait until
+        // they are written before the CTA retires
+        if (warp < 8) {
+          const int rr = (warp - 4) * 32 + lane;
+          const int lrr = row0 + rr;
+          if (lrr < R)
+            bulk_store_global(p.part_o + (size_t(split) * rows_total + size_t(b) * R + lrr) * kDv,
+                              smem_u32(stg + rr * kEpiRowBytes), uint32_t(kDv * 2));
+          bulk_commit();
+          bulk_wait<0>();
+          if (lane == 0 && warp == 4) VA_TRACE_CTA(5, 1);
+        }
+        named_sync(kSoftmaxBar, kSoftmax);
       } else if (ok && !fin) {
         fail();
       }
