@@ -55,6 +55,33 @@ def parse():
     return ap.parse_args()
 
 
+KERNEL_SOURCES = ("va_tc.cu", "va_common.cuh", "va_sm100.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_tc_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mla_speculative_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the split-K kernel on the benchmark workload,
+    from the committed ncu capture -- or None when the kernel sources changed
+    since that capture (the counters no longer describe this kernel)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+
+
 def run_case(va, args, dev):
     """A few plain verify calls of one workload, for profiler captures."""
     H, P, layout = args.case.split(",")
@@ -211,9 +238,13 @@ class Step:
                                   out=self.out, lse=self.lse, stream=stream)
 
 
-def capture_graphs(step: Step, with_events: bool):
-    """One CUDA graph per rotated slot table; optionally with event records
-    around the split-K kernel inside each graph."""
+STEPS_PER_GRAPH = 8
+
+
+def capture_graphs(step: Step, with_events: bool, per_graph: int = 1):
+    """CUDA graphs over the rotated slot tables, `per_graph` consecutive steps
+    (each on its own table) per graph; with events, one step per graph and
+    event records around its split-K kernel."""
     va = step.va
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -223,7 +254,9 @@ def capture_graphs(step: Step, with_events: bool):
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     graphs, evs = [], []
-    for k in range(step.nrot):
+    per_graph = 1 if with_events else max(1, per_graph)
+    ngraphs = max(1, step.nrot // per_graph)
+    for gi in range(ngraphs):
         g = torch.cuda.CUDAGraph()
         if with_events:
             eb = torch.cuda.Event(enable_timing=True)
@@ -231,14 +264,17 @@ def capture_graphs(step: Step, with_events: bool):
             va.set_partial_events(eb, ea)
             evs.append((eb, ea))
         with torch.cuda.graph(g):
-            step.call(k)
+            for j in range(per_graph):
+                step.call(gi * per_graph + j)
         graphs.append(g)
     va.set_partial_events(None, None)
     return graphs, evs
 
 
-def time_graphs(graphs, K, W, dist=None):
-    for k in range(W):
+def time_graphs(graphs, K, W, dist=None, per_graph: int = 1):
+    """Times exactly K steps: K / per_graph replays (K a multiple of per_graph)."""
+    assert K % per_graph == 0 and W >= 1
+    for k in range(max(1, -(-W // per_graph))):
         graphs[k % len(graphs)].replay()
     torch.cuda.synchronize()
     if dist is not None:
@@ -247,7 +283,7 @@ def time_graphs(graphs, K, W, dist=None):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for k in range(K):
+    for k in range(K // per_graph):
         graphs[k % len(graphs)].replay()
     e1.record()
     torch.cuda.synchronize()
@@ -264,14 +300,18 @@ def kernel_ms(evs, used):
 
 
 def measure(step: Step, K: int, W: int, dist=None):
-    """(ms per step, ms of the split-K kernel).  The step time comes from
-    graphs with nothing but the step's kernels, so that each kernel may start
-    while its predecessor finishes (programmatic dependent launch); the kernel
-    time from a second set of graphs with event records around the split-K
-    kernel, replayed after the timed region."""
-    graphs, _ = capture_graphs(step, with_events=False)
+    """(ms for K steps, ms of the split-K kernel).  The step time comes from
+    graphs with nothing but the steps' kernels -- eight consecutive steps, each
+    on its own rotated slot table, per graph, as a serving loop would capture
+    them, so that host-side graph submission does not pace the device -- and
+    each kernel may start while its predecessor finishes (programmatic
+    dependent launch); the kernel time from a second set of one-step graphs
+    with event records around the split-K kernel, replayed after the timed
+    region."""
+    per = STEPS_PER_GRAPH if K % STEPS_PER_GRAPH == 0 and step.nrot >= STEPS_PER_GRAPH else 1
+    graphs, _ = capture_graphs(step, with_events=False, per_graph=per)
     egraphs, evs = capture_graphs(step, with_events=True)
-    ms = time_graphs(graphs, K, W, dist)
+    ms = time_graphs(graphs, K, W, dist, per_graph=per)
     for g in egraphs:
         g.replay()
     for g in egraphs:
@@ -474,7 +514,7 @@ def main():
                 nr = max(1, min(16, math.ceil(3 * l2 / kvb)))
                 st = Step(va, pool, Hs, 16, Ps, seed=7, nrot=nr, dev=dev, path=args.path,
                           nsplit=0, layout=lay)
-                reps = max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8))))
+                reps = 8 * math.ceil(max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8)))) / 8)
                 tms, kms = measure(st, reps, 5)
                 us = tms / reps * 1e3
                 sweep.append({"H": Hs, "T": 16, "P": Ps, "layout": lay, "us_per_step": us,
@@ -502,9 +542,11 @@ def main():
                    "path": ["auto", "fma", "tc"][args.path],
                    "l2": f"inputs larger than L2: {step.nrot} rotating slot tables "
                          f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
-                   "launch": "CUDA graph per step", "parallelism": f"replicas x{world}"},
+                   "launch": f"CUDA graphs of {STEPS_PER_GRAPH} steps, programmatic dependent "
+                             "launch between the kernels of a step",
+                   "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": recorded_traffic(),
                      "kernel": "split-K partial", "kernel_us": k_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk,
