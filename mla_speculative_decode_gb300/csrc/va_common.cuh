@@ -161,6 +161,9 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 #ifdef VA_TRACE
+#ifdef VA_TRACE_NO_EVENTS
+#define VA_TRACE_EVENT(role, ev, t) ((void)0)
+#else
 #define VA_TRACE_EVENT(role, ev, t)                                                        \
   do {                                                                                   \
     if (g_va_trace && blockIdx.x < 2 && blockIdx.y == 0 && blockIdx.z == 0 && (t) < 512) { \
@@ -169,6 +172,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
       g_va_trace[((role) * 8 + (ev)) * 512 + (t)] = _ts;                                  \
     }                                                                                    \
   } while (0)
+#endif
 // Per-cluster marks of the partial kernel: slot (role, ev, cluster index).
 #define VA_TRACE_CTA(role, ev)                                                             \
   do {                                                                                     \
@@ -178,9 +182,27 @@ __device__ __forceinline__ void griddep_launch_dependents() {
       g_va_trace[((role) * 8 + (ev)) * 512 + (blockIdx.x >> 1)] = _ts;                      \
     }                                                                                      \
   } while (0)
+// Phase clocks: a role accumulates clock64 deltas per phase over all tiles
+// in registers and stores the sums once, into roles 8-15 of the buffer.
+#define VA_PH_DECL long long _ph[8] = {0, 0, 0, 0, 0, 0, 0, 0}; long long _pt = clock64()
+#define VA_PH(i)                                                                           \
+  do {                                                                                     \
+    const long long _n = clock64();                                                        \
+    _ph[i] += _n - _pt;                                                                     \
+    _pt = _n;                                                                              \
+  } while (0)
+#define VA_PH_STORE(role)                                                                  \
+  do {                                                                                     \
+    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && (blockIdx.x >> 1) < 512)       \
+      for (int _i = 0; _i < 8; ++_i)                                                       \
+        g_va_trace[((role) * 8 + _i) * 512 + (blockIdx.x >> 1)] = (unsigned long long)_ph[_i]; \
+  } while (0)
 #else
 #define VA_TRACE_EVENT(role, ev, t) ((void)0)
 #define VA_TRACE_CTA(role, ev) ((void)0)
+#define VA_PH_DECL ((void)0)
+#define VA_PH(i) ((void)0)
+#define VA_PH_STORE(role) ((void)0)
 #endif
 
 // Launchers (defined in the kernel translation units).

@@ -200,6 +200,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   int raw = ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
   bool bad_slot = false;
+  VA_PH_DECL;
   for (int t = 0; t < ntiles; ++t) {
     const int g0 = kBlocks * t;   // ring position of the tile's first block
     const int s0 = g0 % kRing;
@@ -218,6 +219,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
                         kWaitCycles);
     }
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
+    VA_PH(0);
     if (ptid < 64) {
       const int rw = checked_row(p, raw);
       srow[(t & 1) * 64 + ptid] = rw;
@@ -232,6 +234,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
       ok = false;
       break;
     }
+    VA_PH(1);
     const uint32_t fb = full0 + 8u * uint32_t(t & 1);
     // contiguous rows, whole tile inside the split and the pool: box loads
     const int tk0 = sr.k0 + t * kTile;
@@ -282,7 +285,9 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     }
     cp_async_arrive_noinc(fb);
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
+    VA_PH(2);
   }
+  if (ptid == 0) VA_PH_STORE(kMask ? 11 : 12);
   cp_async_wait_all();
   if (kMask && bad_slot) {
     griddep_wait();
@@ -421,12 +426,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QREADY), 0, abort_flag, kWaitCycles));
       if (!ok && lane == 0) fail();
       constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+      VA_PH_DECL;
       for (int t = 0; ok && t < ntiles; ++t) {
         const int bs = t & 1;
         const bool got =
             mbar_wait(bar(B_FULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
             (t < 2 || mbar_wait(bar(B_SEMPTY + bs), uint32_t((t >> 1) - 1) & 1u, abort_flag,
                                 kWaitCycles));
+        VA_PH(0);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) fail();
           break;
@@ -453,7 +460,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mma_commit_warp(bar(B_SFULL + bs));
         if (lane == 0) VA_TRACE_EVENT(1, 1, t);
+        VA_PH(2);
       }
+      if (lane == 0) VA_PH_STORE(9);
       mma_commit_warp(bar(B_MMAFIN));
       mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
       __syncwarp();
@@ -482,6 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       bool issuer_ok = true;
       bool ok = true;
+      VA_PH_DECL;
       for (int t = 0; t < ntiles; ++t) {
         const int bs = t & 1;             // S buffer and staging buffer
         const int pb = t % kPBufs;        // P buffer of the PV CTA
@@ -503,6 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait(bar(B_SFULL + bs), uint32_t(t >> 1) & 1u, abort_flag, kWaitCycles) &&
             mbar_wait(bar(B_VREADY + t % kValidRing), uint32_t(t / kValidRing) & 1u, abort_flag,
                       kWaitCycles);
+        VA_PH(0);
         const bool wok = __all_sync(0xffffffffu, got);
         float x[32];
         float mth = -INFINITY;
@@ -521,6 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mth = fmaxf(mth, x[c]);
           }
         }
+        VA_PH(1);
         mx[half * kRows + r] = mth;
         if (issuer) bulk_wait_read<1>();   // staging buffer bs: tile t-2's copy has read it
         if (!named_sync_and(kSoftmaxBar, kSoftmax, wok && issuer_ok)) {
@@ -528,6 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        VA_PH(2);
         const float mt = fmaxf(mx[r], mx[kRows + r]);
         float alpha = 1.f;
         if (mt > m_ref + kRescaleLog2) {
@@ -541,6 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 16; ++c)
           pk[c] = pack_bf16(ex2_approx(x[2 * c] - mr), ex2_approx(x[2 * c + 1] - mr), l);
         if (tid == 128) VA_TRACE_EVENT(2, 1, t);
+        VA_PH(3);
         // this row's 32 keys into the staging buffer (K-major, 128B swizzle)
         uint8_t* stg = gb + kOffStage + uint32_t(bs) * kPBufBytes;
 #pragma unroll
@@ -556,7 +570,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint32_t*>(stg + kPFlags)[q4] = (uint32_t(t) << 1) | (wres ? 1u : 0u);
         }
         fence_proxy_async_cta();   // staging writes, read by the bulk copy
+        VA_PH(4);
         named_sync(kSoftmaxBar, kSoftmax);
+        VA_PH(5);
         if (issuer) {
           issuer_ok = t < kPBufs ||
                       mbar_wait<true>(bar(B_PFREE + pb), uint32_t((t / kPBufs) - 1) & 1u,
@@ -570,7 +586,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (tid == 128) VA_TRACE_EVENT(2, 3, t);
         }
+        VA_PH(6);
       }
+      if (tid == 128) VA_PH_STORE(8);
       // row sums: the two warpgroups' partial sums share the reference max
       if (ok) {
         mx[half * kRows + r] = l;
@@ -615,6 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kPBufs && t < ntiles; ++t)
           mbar_arrive_expect_tx(bar(B_PFULL + t), kPPayload);
       __syncwarp();
+      VA_PH_DECL;
       for (int t = 0; t < ntiles; ++t) {
         const int bs = t % kPBufs;
         const bool got =
@@ -625,6 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) VA_TRACE_EVENT(4, 0, t);
+        VA_PH(0);
         const uint32_t pbase = sb + kOffP + uint32_t(bs) * kPBufBytes;
         const volatile uint32_t* flags =
             reinterpret_cast<const volatile uint32_t*>(gb + kOffP + bs * kPBufBytes + kPFlags);
@@ -652,6 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        VA_PH(1);
         fence_proxy_async_cta();
         tc_fence_after();
         const uint64_t ad0 = smem_desc(pbase, 16, 1024, kSwizzle128B);
@@ -680,7 +701,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         mma_commit_mc_warp(bar(B_PFREE + bs), uint16_t(1u << 0));
         if (lane == 0) VA_TRACE_EVENT(4, 1, t);
+        VA_PH(2);
       }
+      if (lane == 0) VA_PH_STORE(10);
       // last command to the row warps: no more rescales
       if (lane == 0) {
         *cmd = kCmdDone;
