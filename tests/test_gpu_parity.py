@@ -374,3 +374,56 @@ def test_defrag_bad_rows_flagged_not_written(va):
     assert int(status.item()) == va.STATUS_BAD_SLOT | va.STATUS_BAD_DST
     assert torch.equal(pool[254], before[3])
     assert torch.equal(pool[:254], before[:254]) and torch.equal(pool[255], before[255])
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+def test_status_is_per_call_back_to_back(va, path):
+    """The status word belongs to the last call: the split-K kernel may start
+    while the tree-mask kernel (which clears the word) still runs, so every
+    status write of the split-K kernel must come after it.  Calls go back to
+    back on one stream, alternating inputs with and without bad slots, with no
+    host synchronisation between them; the word is read after each pair and
+    inside one captured graph."""
+    s = synth.Spec("pc", B=1, H=8, T=16, prefix=[2000], num_slots=8192, seed=61)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    d_ok = _gpu.to_device(w)
+    d_bad = dict(d_ok)
+    bad = w.slot_idx.clone()
+    bad[3] = 8192 + 11
+    bad[1500] = -2
+    d_bad["slot_idx"] = bad.cuda()
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, 0, path)
+    out = torch.empty(s.T, s.H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(s.T, s.H, dtype=torch.float32, device="cuda")
+
+    def call(dd):
+        va.verify_attn_paged(dd["q"], dd["kv_pool"], dd["slot_idx"], dd["kv_indptr"],
+                             dd["prefix_len"], dd["parents"], sm_scale=s.sm_scale, nsplit=ns,
+                             flags=path, workspace=ws, out=out, lse=lse)
+
+    for _ in range(10):
+        call(d_bad)
+        call(d_ok)
+        assert va.read_status(ws) == 0
+        call(d_ok)
+        call(d_bad)
+        assert va.read_status(ws) == va.STATUS_BAD_SLOT
+
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        call(d_ok)
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    for first, second, want in ((d_bad, d_ok, 0), (d_ok, d_bad, va.STATUS_BAD_SLOT)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call(first)
+            call(second)
+        for _ in range(5):
+            g.replay()
+            assert va.read_status(ws) == want
+    ref_o, ref_l = _gpu.reference(w)
+    call(d_ok)
+    _gpu.compare(out, lse, ref_o, ref_l)
