@@ -197,16 +197,20 @@ def device_pool(num_slots: int, seed: int, dev) -> torch.Tensor:
 class Step:
     """Device-resident inputs of one verify step plus `nrot` rotated slot tables
     (disjoint random subsets of the pool) so that consecutive steps read rows
-    that are not in L2."""
+    that are not in L2.  `P` is one prefix length or a list, one per request
+    (requests take disjoint slots of the shared pool)."""
 
     def __init__(self, va, pool, H, T, P, seed, nrot, dev, path, nsplit, layout="scattered"):
         self.va = va
         self.pool = pool
-        self.H, self.T, self.P = H, T, P
-        self.N = P + T
+        prefixes = [int(P)] if isinstance(P, int) else [int(x) for x in P]
+        B = len(prefixes)
+        self.B, self.H, self.T, self.P = B, H, T, prefixes[0]
+        Ns = [x + T for x in prefixes]
+        self.N = sum(Ns)
         g = torch.Generator().manual_seed(seed)
-        self.q = (torch.randn(T, H, synth.D_QK, generator=g)).to(torch.bfloat16).to(dev)
-        self.parents = synth.make_parents(T, "random", g).view(1, T).to(dev)
+        self.q = (torch.randn(B * T, H, synth.D_QK, generator=g)).to(torch.bfloat16).to(dev)
+        self.parents = torch.stack([synth.make_parents(T, "random", g) for _ in range(B)]).to(dev)
         perm = torch.randperm(pool.shape[0], generator=g)
         if nrot * self.N > pool.shape[0]:
             nrot = max(1, pool.shape[0] // self.N)
@@ -214,16 +218,22 @@ class Step:
         self.layout = layout
         self.tables = [perm[k * self.N:(k + 1) * self.N].to(torch.int32).to(dev)
                        for k in range(nrot)]
-        # contiguous layout: rotation k reads pool rows [k*N, (k+1)*N)
-        self.starts = [torch.tensor([k * self.N], dtype=torch.int64, device=dev)
-                       for k in range(nrot)]
-        self.indptr = torch.tensor([0, self.N], dtype=torch.int32, device=dev)
-        self.prefix = torch.tensor([P], dtype=torch.int32, device=dev)
+        offs = [0]
+        for n in Ns:
+            offs.append(offs[-1] + n)
+        # contiguous layout: rotation k reads pool rows [k*N, (k+1)*N), request
+        # b from k*N + offs[b]
+        self.starts = [torch.tensor([k * self.N + o for o in offs[:-1]], dtype=torch.int64,
+                                    device=dev) for k in range(nrot)]
+        self.indptr = torch.tensor(offs, dtype=torch.int32, device=dev)
+        self.prefix = torch.tensor(prefixes, dtype=torch.int32, device=dev)
         self.path = path
-        self.ws, self.nsplit = va.alloc_workspace(1, T, H, nsplit, path, dev)
-        self.out = torch.empty(T, H, synth.D_V, dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+        self.ws, self.nsplit = va.alloc_workspace(B, T, H, nsplit, path, dev)
+        self.out = torch.empty(B * T, H, synth.D_V, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(B * T, H, dtype=torch.float32, device=dev)
         self.kv_bytes = self.N * synth.D_QK * 2
+        # tensor-core work: 2176 flop (2*576 + 2*512) for every row and every key
+        self.flops = sum(2176.0 * T * H * n for n in Ns)
 
     def call(self, k, stream=None):
         if self.layout == "contiguous":
@@ -297,6 +307,25 @@ def kernel_ms(evs, used):
     """Average split-K kernel duration over the last replay of each graph used."""
     n = min(len(evs), used)
     return float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in range(n)]))
+
+
+def measure_dist(step: Step, K: int, W: int, runs: int = 5):
+    """Per-step µs of `runs` timed runs of K steps each: (median, p10, p90), and
+    the split-K kernel µs."""
+    per = STEPS_PER_GRAPH if K % STEPS_PER_GRAPH == 0 and step.nrot >= STEPS_PER_GRAPH else 1
+    graphs, _ = capture_graphs(step, with_events=False, per_graph=per)
+    egraphs, evs = capture_graphs(step, with_events=True)
+    vals = [time_graphs(graphs, K, W if i == 0 else 1, None, per_graph=per) / K * 1e3
+            for i in range(runs)]
+    for g in egraphs:
+        g.replay()
+    for g in egraphs:
+        g.replay()
+    torch.cuda.synchronize()
+    k_us = kernel_ms(evs, len(egraphs)) * 1e3
+    del graphs, egraphs
+    v = np.array(vals)
+    return float(np.median(v)), float(np.percentile(v, 10)), float(np.percentile(v, 90)), k_us
 
 
 def measure(step: Step, K: int, W: int, dist=None):
@@ -549,16 +578,67 @@ def main():
                 st = Step(va, pool, Hs, 16, Ps, seed=7, nrot=nr, dev=dev, path=args.path,
                           nsplit=0, layout=lay)
                 reps = 8 * math.ceil(max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8)))) / 8)
-                tms, kms = measure(st, reps, 5)
-                us = tms / reps * 1e3
+                us, p10, p90, k_us = measure_dist(st, reps, 5)
                 sweep.append({"H": Hs, "T": 16, "P": Ps, "layout": lay, "us_per_step": us,
+                              "p10": p10, "p90": p90,
                               "gbs": kvb / (us * 1e-6) / 1e9,
                               "frac_hbm": kvb / (us * 1e-6) / 1e9 / hbm_peak,
-                              "partial_kernel_us": kms * 1e3,
-                              "partial_gbs": kvb / (kms * 1e-3) / 1e9, "nsplit": st.nsplit,
+                              "tflops": st.flops / (us * 1e-6) / 1e12,
+                              "partial_kernel_us": k_us,
+                              "partial_gbs": kvb / (k_us * 1e-6) / 1e9, "nsplit": st.nsplit,
                               "path": "auto" if args.path == 0 else str(args.path)})
                 del st
                 torch.cuda.empty_cache()
+
+    # ---- the remaining configurations of the step, and the defrag compaction
+    configs = {}
+    if not args.no_sweep and rank == 0:
+        # long context: H=8, T=32 random tree, prefix 200000, 2^18-slot pool,
+        # nsplit swept (two 128-row blocks per split)
+        pool_l = device_pool(1 << 18, seed=3, dev=dev)
+        rows = []
+        for ns in (16, 32, 64, 96, 128, 0):
+            st = Step(va, pool_l, 8, 32, 200000, seed=3, nrot=1, dev=dev, path=args.path, nsplit=ns)
+            med, p10, p90, k_us = measure_dist(st, 16, 3)
+            rows.append({"nsplit": st.nsplit, "auto": ns == 0, "us_per_step": med, "p10": p10,
+                         "p90": p90, "gbs": st.kv_bytes / (med * 1e-6) / 1e9,
+                         "tflops": st.flops / (med * 1e-6) / 1e12, "partial_kernel_us": k_us})
+            del st
+        configs["long H=8 T=32 P=200000 scattered (2^18 pool)"] = rows
+        del pool_l
+        torch.cuda.empty_cache()
+        # batched ragged: 8 requests, prefixes U[1024, 65536], H=64, T=16
+        prefs = synth.spec("batched").prefix
+        st = Step(va, pool, 64, 16, prefs, seed=4, nrot=2, dev=dev, path=args.path, nsplit=0)
+        med, p10, p90, k_us = measure_dist(st, 8, 3)
+        configs["batched B=8 H=64 T=16 ragged, one graph per step"] = {
+            "prefixes": prefs, "nsplit": st.nsplit, "us_per_step": med, "p10": p10, "p90": p90,
+            "gbs": st.kv_bytes / (med * 1e-6) / 1e9, "tflops": st.flops / (med * 1e-6) / 1e12,
+            "partial_kernel_us": k_us, "kv_bytes": st.kv_bytes}
+        del st
+        torch.cuda.empty_cache()
+        # defrag: 65536 scattered rows (lower half of the pool) compacted into a
+        # contiguous range in the upper half
+        gd = torch.Generator().manual_seed(7)
+        n = 65536
+        src = torch.randperm(pool.shape[0] // 2, generator=gd)[:n].to(torch.int32).to(dev)
+        sind = torch.tensor([0, n], dtype=torch.int32, device=dev)
+        dstb = torch.tensor([pool.shape[0] // 2], dtype=torch.int64, device=dev)
+        for _ in range(3):
+            va.verify_attn_defrag(pool, src, sind, dstb)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        e0.record()
+        for _ in range(reps):
+            va.verify_attn_defrag(pool, src, sind, dstb)
+        e1.record()
+        torch.cuda.synchronize()
+        d_us = e0.elapsed_time(e1) / reps * 1e3
+        moved = 2 * n * synth.D_QK * 2
+        configs["defrag 65536 scattered rows -> contiguous"] = {
+            "us": d_us, "bytes_moved": moved, "gbs": moved / (d_us * 1e-6) / 1e9,
+            "frac_hbm": moved / (d_us * 1e-6) / 1e9 / hbm_peak}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -584,7 +664,7 @@ def main():
                      "kernel": "split-K partial", "kernel_us": k_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk,
-        "parity": parity, "sweep": sweep,
+        "parity": parity, "sweep": sweep, "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -818,14 +818,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 bool tc_supported(int, int, int) { return true; }
 
-// Splits per (row block, request) so that all clusters are co-resident:
-// `pairs` is the number of two-CTA clusters the device runs at once (clusters
-// live inside one GPC, so GPCs with an odd SM count strand an SM, and a grid
-// of num_sms / 2 clusters would leave a second, nearly empty wave).
+// Splits per (row block, request).  `pairs` is the number of two-CTA clusters
+// the device runs at once (clusters live inside one GPC, so GPCs with an odd
+// SM count strand an SM).  With few (row block, request) items, one wave of
+// clusters splits each item evenly.  With many (more than half a wave), one
+// split per item would leave clusters idle and let the longest request of a
+// ragged batch set the time, so the items are split into about three waves
+// of clusters instead.  (Prefix lengths live on the device, so the rule uses
+// the shape only; splits past a request's keys exit at once.)
 int tc_auto_nsplit(int B, int T, int H, int pairs) {
   const long rowblocks = (long(T) * H + kRows - 1) / kRows;
   const long items = rowblocks * B;
-  long ns = pairs / items;
+  long ns = 2 * items <= pairs ? pairs / items : (3 * pairs + items - 1) / items;
   if (ns < 1) ns = 1;
   if (ns > VA_NSPLIT_MAX) ns = VA_NSPLIT_MAX;
   return int(ns);
