@@ -140,6 +140,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 
 constexpr int kDefragThreads = 256;
 
+// A warp moves four rows per round: the four source slots arrive with one
+// load, then every chunk of the four rows is loaded before any is stored, so
+// a round pays the memory latency about twice rather than twice per row.
+constexpr int kDefragRows = 4;
+
 __global__ void __launch_bounds__(kDefragThreads)
     defrag_kernel(uint4* pool, int64_t num_slots, int64_t vec_per_row, const int32_t* src,
                   const int32_t* indptr, const int64_t* dst_base, int32_t* slots_out,
@@ -150,22 +155,53 @@ __global__ void __launch_bounds__(kDefragThreads)
   const int64_t nwarps = int64_t(gridDim.x) * (kDefragThreads / 32);
   const int64_t i0 = indptr[b], n = int64_t(indptr[b + 1]) - i0;
   const int64_t dbase = dst_base[b];
-  for (int64_t i = warp; i < n; i += nwarps) {
-    int64_t s = 0;
-    if (lane == 0) s = src[i0 + i];
-    s = __shfl_sync(0xffffffffu, s, 0);
-    const int64_t d = dbase + i;
-    const bool s_ok = s >= 0 && s < num_slots;
-    const bool d_ok = d >= 0 && d < num_slots;
-    if (!s_ok || !d_ok) {
-      if (lane == 0 && status)
+  for (int64_t r0 = warp * kDefragRows; r0 < n; r0 += nwarps * kDefragRows) {
+    const int64_t s_lane = (lane < kDefragRows && r0 + lane < n) ? int64_t(src[i0 + r0 + lane]) : 0;
+    bool ok[kDefragRows];
+    int64_t sr[kDefragRows];
+#pragma unroll
+    for (int k = 0; k < kDefragRows; ++k) {
+      const int64_t i = r0 + k;
+      const int64_t s = __shfl_sync(0xffffffffu, s_lane, k);
+      const int64_t d = dbase + i;
+      const bool s_ok = s >= 0 && s < num_slots;
+      const bool d_ok = d >= 0 && d < num_slots;
+      sr[k] = s;
+      ok[k] = i < n && s_ok && d_ok;
+      if (i < n && !(s_ok && d_ok) && lane == 0 && status)
         atomicOr(status, (s_ok ? 0u : VA_STATUS_BAD_SLOT) | (d_ok ? 0u : VA_STATUS_BAD_DST));
-      continue;
     }
-    const uint4* from = pool + s * vec_per_row;
-    uint4* to = pool + d * vec_per_row;
-    for (int64_t c = lane; c < vec_per_row; c += 32) to[c] = from[c];
-    if (lane == 0 && slots_out) slots_out[i0 + i] = int32_t(d);
+    if (vec_per_row <= 96) {
+      uint4 v[kDefragRows][3];
+#pragma unroll
+      for (int k = 0; k < kDefragRows; ++k)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int64_t c = lane + 32 * j;
+          if (ok[k] && c < vec_per_row) v[k][j] = pool[sr[k] * vec_per_row + c];
+        }
+#pragma unroll
+      for (int k = 0; k < kDefragRows; ++k)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int64_t c = lane + 32 * j;
+          if (ok[k] && c < vec_per_row) pool[(dbase + r0 + k) * vec_per_row + c] = v[k][j];
+        }
+    } else {
+      for (int k = 0; k < kDefragRows; ++k) {
+        if (!ok[k]) continue;
+        const uint4* from = pool + sr[k] * vec_per_row;
+        uint4* to = pool + (dbase + r0 + k) * vec_per_row;
+        for (int64_t c = lane; c < vec_per_row; c += 32) to[c] = from[c];
+      }
+    }
+    if (lane < kDefragRows && r0 + lane < n && slots_out) {
+      bool okl = false;
+#pragma unroll
+      for (int k = 0; k < kDefragRows; ++k)
+        if (k == lane) okl = ok[k];
+      if (okl) slots_out[i0 + r0 + lane] = int32_t(dbase + r0 + lane);
+    }
   }
 }
 
@@ -194,7 +230,8 @@ cudaError_t launch_defrag(void* pool, int64_t num_slots, int64_t stride, const i
                           const int32_t* indptr, const int64_t* dst_base, int32_t* slots_out,
                           int B, int64_t max_rows, uint32_t* status, cudaStream_t st) {
   const int64_t per_req = (max_rows + B - 1) / B;
-  int64_t blocks = (per_req + 4 * (kDefragThreads / 32) - 1) / (4 * (kDefragThreads / 32));
+  int64_t blocks = (per_req + kDefragRows * (kDefragThreads / 32) - 1) /
+                   (kDefragRows * (kDefragThreads / 32));
   if (blocks < 1) blocks = 1;
   if (blocks > 65535) blocks = 65535;
   dim3 grid{unsigned(blocks), unsigned(B), 1u};
