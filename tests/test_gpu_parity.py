@@ -362,6 +362,30 @@ def test_defrag_byte_exact_and_attention_preserved(va):
     assert torch.equal(out0, out2) and torch.equal(lse0, lse2)
 
 
+@pytest.mark.parametrize("stride", [576, 640, 1152])
+def test_defrag_row_strides_byte_exact(va, stride):
+    """Whole rows of any stride move byte for byte: rows of at most 96 16-byte
+    chunks go through the four-rows-per-round path, wider rows through the
+    chunk loop; a ragged last round of each request included."""
+    n_slots = 4096
+    g = torch.Generator().manual_seed(63 + stride)
+    pool = synth._bf16_normal((2 * n_slots, stride), g)
+    src = torch.randperm(n_slots, generator=g)[:701].to(torch.int32)
+    indptr = torch.tensor([0, 303, 701], dtype=torch.int32)
+    dst = torch.tensor([n_slots + 5, n_slots + 400], dtype=torch.int64)
+    ref_pool, ref_slots = oracle.defrag(synth.as_u16(pool), src.numpy(),
+                                        indptr.numpy().astype(np.int64), dst.numpy())
+    dpool = pool.cuda()
+    new_slots = src.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    va.verify_attn_defrag(dpool, src.cuda(), indptr.cuda(), dst.cuda(), slot_idx_out=new_slots,
+                          status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    np.testing.assert_array_equal(dpool.cpu().view(torch.int16).numpy().view(np.uint16), ref_pool)
+    np.testing.assert_array_equal(new_slots.cpu().numpy(), ref_slots)
+
+
 def test_defrag_bad_rows_flagged_not_written(va):
     pool = torch.randn(256, 576).to(torch.bfloat16).cuda()
     before = pool.clone()
