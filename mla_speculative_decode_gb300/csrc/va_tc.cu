@@ -101,7 +101,8 @@ enum : int {
   B_QREADY = B_PFULL + kPBufs,
   B_MMAFIN, B_OGO, B_OCORR, B_ODONE, B_FIN,
   B_VREADY,                   // [kValidRing] key-validity masks (QK CTA)
-  kNumBars = B_VREADY + kValidRing
+  B_QTMA = B_VREADY + kValidRing,   // Q rows landed in shared memory (QK CTA)
+  kNumBars
 };
 
 // shared layout (offsets from a 1024-byte aligned base)
@@ -115,6 +116,12 @@ constexpr uint32_t kOffSrow = 1536;                         // int32 [2][64] sta
 constexpr uint32_t kOffMx = 2048;                           // QK: float [2][128] half maxima
 constexpr uint32_t kOffK = 4096;                            // QK: K ring
 constexpr uint32_t kOffStage = kOffK + kRingK * kBlockBytes;   // QK: P staging [2]
+// QK: the row block's Q (128 rows x 576 features, two boxes of 64 rows laid
+// out [column block][row][128 B], 128B-swizzled), loaded once at the start
+// into ring slots 9..22 and the staging buffers, which the first tile (slots
+// 0..8) does not use; it stays there until the rows are in TMEM.
+constexpr uint32_t kOffQ = kOffK + kKBlocks * kBlockBytes;
+constexpr uint32_t kQBoxBytes = 64u * kDqk * 2u;            // 64 rows, 72 KB
 constexpr uint32_t kOffP = 4096;                            // PV: P buffers [kPBufs]
 constexpr uint32_t kOffV = kOffP + kPBufs * kPBufBytes;     // PV: V ring
 constexpr uint32_t kEndQK = kOffStage + 2 * kPBufBytes;
@@ -125,7 +132,10 @@ constexpr uint32_t kEndPV = kOffV + kRingV * kBlockBytes;
 constexpr uint32_t kSmemBytes = (kEndQK > kEndPV ? kEndQK : kEndPV) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffP + 128 * kEpiRowBytes <= kEndPV, "epilogue staging");
-static_assert(8 * 4096 <= 2 * kPBufBytes, "Q load scratch in the P staging buffers");
+static_assert(kOffQ % 1024 == 0 && kOffQ + 2 * kQBoxBytes <= kEndQK, "Q landing area");
+// Tile 1 (slots 9..17) is the only tile whose slots hold Q and have no earlier
+// occupant to wait for; tile 2 wraps around to slots released by tile 0.
+static_assert(2 * kKBlocks <= kRingK && 3 * kKBlocks > kRingK, "Q area against the K ring");
 static_assert(8 * kNumBars <= int(kOffTmemSlot), "barrier area");
 static_assert(kOffValid + 8 * kValidRing <= kOffFin && kOffMx + 1024 <= kOffK, "header");
 // The key-validity masks travel through their own ring of kValidRing
@@ -194,10 +204,9 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
                                         uint32_t empty0, int* srow, uint32_t* valid32,
                                         uint32_t vready0, volatile int* abort_flag,
                                         const CUtensorMap* map3, const CUtensorMap* map2,
-                                        bool box3d) {
+                                        bool box3d, uint32_t qready, int raw) {
   constexpr int kChunks = kBlocks * 8;
   const int lane = ptid & 31;
-  int raw = ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
   bool ok = true;
   bool bad_slot = false;
   VA_PH_DECL;
@@ -217,6 +226,8 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
       if (ptid == 0 && g >= kRing)
         got = mbar_wait(empty0 + 8u * uint32_t(g % kRing), uint32_t(g / kRing - 1) & 1u, abort_flag,
                         kWaitCycles);
+      // QK side: tile 1's slots hold Q until its rows are in TMEM
+      if (kMask && ptid == 0 && t == 1) got = mbar_wait(qready, 0, abort_flag, kWaitCycles);
     }
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
     VA_PH(0);
@@ -296,61 +307,42 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   return ok;
 }
 
-// Q rows into TMEM as the A operand (bf16 pairs, 288 columns).  The two
+// Q rows into TMEM as the A operand (bf16 pairs, 288 columns), from the
+// shared landing area that the row block's two TMA boxes filled.  The two
 // softmax warpgroups share the work: warp w writes lane quadrant w%4 (rows
-// 32*(w%4) .. +31) for column chunks 0-4 (first warpgroup) or 5-8 (second),
-// 64 features (128 bytes) per chunk.  Global reads are coalesced -- one warp
-// instruction reads 128 contiguous bytes of each of four rows -- and go
-// through the warp's own 4 KB of shared scratch (`scratch`, 128B-swizzled
-// rows) so that lane r then holds row r's chunk for tcgen05.st.  Two chunks
-// are in flight per round trip to memory.
-__device__ __forceinline__ void load_q(const Params& p, int b, int row0, int half, int q4, int lane,
-                                       uint32_t tmem, uint8_t* scratch) {
+// 32*(w%4) .. +31) for column blocks 0-4 (first warpgroup) or 5-8 (second).
+// Lane r reads its row's 128-byte piece of a column block as eight 16-byte
+// chunks (chunk j sits at position j ^ (r%8) of the swizzled row) and stores
+// it with one tcgen05.st.  Returns false when the bounded wait for the boxes
+// gave up.
+__device__ __forceinline__ bool load_q(int half, int q4, int lane, uint32_t tmem, uint32_t qs,
+                                       uint32_t qbar, volatile int* abort_flag) {
+  const bool ok = mbar_wait(qbar, 0, abort_flag, kWaitCycles);
   const int c_begin = half ? 5 : 0, c_end = half ? 9 : 5;
   const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16) + kTmemQ;
-  const int sub = lane >> 3, piece = lane & 7;   // row within a group of 4, 16-byte piece
+  const int r = q4 * 32 + lane;   // row of the block
+  const uint32_t row_addr = qs + uint32_t(r >> 6) * kQBoxBytes + uint32_t(r & 63) * 128u;
+  if (ok) {
 #pragma unroll 1
-  for (int c0 = c_begin; c0 < c_end; c0 += 2) {
-    const int n = c_end - c0 < 2 ? c_end - c0 : 2;
-    uint4 buf[2][8];
+    for (int c = c_begin; c < c_end; ++c) {
+      uint32_t v[32];
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int lr = row0 + q4 * 32 + 4 * i + sub;
-        buf[cc][i] = (cc < n && lr < p.rows_per_req)
-                         ? *reinterpret_cast<const uint4*>(
-                               p.q + (size_t(b) * p.rows_per_req + lr) * kDqk + (c0 + cc) * 64 +
-                               piece * 8)
-                         : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 8; ++j) {
+        const uint4 w = ld_shared_v4(row_addr + uint32_t(c) * kBlockBytes + uint32_t((j ^ (r & 7)) * 16));
+        v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
       }
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      if (cc < n) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + sub;
-          *reinterpret_cast<uint4*>(scratch + rr * 128 + ((piece ^ (rr & 7)) * 16)) = buf[cc][i];
-        }
-        __syncwarp();
-        uint32_t v[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(scratch + lane * 128 + ((j ^ (lane & 7)) * 16));
-          v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
-        }
-        __syncwarp();
-        tmem_st32(tl + 32u * uint32_t(c0 + cc), v);
-      }
+      tmem_st32(tl + 32u * uint32_t(c), v);
     }
   }
   tmem_wait_st();
+  return ok;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v,
-                      const __grid_constant__ CUtensorMap tmap_2d, int box3d) {
+                      const __grid_constant__ CUtensorMap tmap_2d,
+                      const __grid_constant__ CUtensorMap tmap_q, int box3d) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -362,6 +354,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int split = blockIdx.x >> 1, rb = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 0);
+  // the maps' descriptors are fetched while the request's bounds load
+  if (tid == 0) {
+    if (rank == 0) tma_prefetch(&tmap_q);
+    if (p.kv_start) {
+      tma_prefetch(rank == 0 ? &tmap_k : &tmap_v);
+      tma_prefetch(&tmap_2d);
+    }
+  }
 
   griddep_launch_dependents();   // the merge kernel may be scheduled as clusters retire
   // The tree-mask kernel before this one clears the status word and writes
@@ -374,6 +374,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int row0 = rb * kRows;
   const int ntiles = ceil_div(sr.k1 - sr.k0, kTile);
   const size_t rows_total = size_t(p.B) * R;
+
+  const bool producer = warp == 0 || warp == 2 || warp == 3 || warp >= 12;
+  const int ptid = warp == 0 ? lane : (warp < 4 ? warp - 1 : warp - 9) * 32 + lane;
+  // raw pool rows of the first tile (producers), loaded during the set-up
+  const int raw0 = producer && ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -393,16 +398,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) tmem_alloc(sb + kOffTmemSlot, kTmemCols);
-  if (tid == 0 && p.kv_start) {
-    tma_prefetch(rank == 0 ? &tmap_k : &tmap_v);
-    tma_prefetch(&tmap_2d);
-  }
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + kOffTmemSlot);
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 1);
-  const bool producer = warp == 0 || warp == 2 || warp == 3 || warp >= 12;
-  const int ptid = warp == 0 ? lane : (warp < 4 ? warp - 1 : warp - 9) * 32 + lane;
   int* srow = reinterpret_cast<int*>(gb + kOffSrow);
   const int half = (warp - 4) >> 2;   // softmax / row warpgroup (warps >= 4)
   const int q4 = warp & 3;            // TMEM lane quadrant of the warp
@@ -416,10 +415,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            bar(B_EMPTY), srow,
                                            reinterpret_cast<uint32_t*>(gb + kOffValid),
                                            bar(B_VREADY), abort_flag, &tmap_k, &tmap_2d,
-                                           box3d != 0) &&
+                                           box3d != 0, bar(B_QREADY), raw0) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
+      // The row block's Q: two boxes of 64 rows x 9 column blocks (rows past
+      // the tensor read as zeros; rows of the next request are never used).
+      // Issued here, after the cluster barrier: issued before it, the copy
+      // in flight held the barrier back by about half a microsecond.
+      if (lane == 0) {
+        const int qrow = b * R + row0;
+        mbar_arrive_expect_tx(bar(B_QTMA), 2u * kQBoxBytes);
+        tma_load_3d(sb + kOffQ, &tmap_q, 0, qrow, 0, bar(B_QTMA));
+        tma_load_3d(sb + kOffQ + kQBoxBytes, &tmap_q, 0, qrow + 64, 0, bar(B_QTMA));
+      }
+      __syncwarp();
       // ---- MMA issuer: S[t%2] = Q K_t^T.  The whole warp runs the loop and
       // one elected lane issues, 36 MMAs back to back with fixed descriptor
       // offsets, so the tensor pipe sees them at its own rate.
@@ -469,9 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
       // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of
       // every tile for row r
-      // the P staging buffers are free until the first tile: 4 KB of Q
-      // transposition scratch per softmax warp
-      load_q(p, b, row0, half, q4, lane, tmem, gb + kOffStage + uint32_t(warp - 4) * 4096u);
+      if (!load_q(half, q4, lane, tmem, sb + kOffQ, bar(B_QTMA), abort_flag) && tid == 128) fail();
       tc_fence_before();
       mbar_arrive(bar(B_QREADY));
       griddep_wait();   // ancestor masks written, status cleared
@@ -620,9 +628,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- producers: value columns of the same tiles
       if (!produce<kVBlocks, kRingV, false>(p, ri, sr, ntiles, ptid, sb + kOffV, bar(B_FULL),
                                             bar(B_EMPTY), srow, nullptr, 0u, abort_flag, &tmap_v,
-                                            &tmap_2d, box3d != 0) &&
+                                            &tmap_2d, box3d != 0, 0u, raw0) &&
           ptid == 0)
         fail();
+      cluster_arrive_relaxed();   // done with the QK CTA (see the end of the kernel)
     } else if (warp == 1) {
       // ---- MMA issuer: O += P_t V_t (whole warp, one elected lane issues)
       constexpr uint32_t idesc = idesc_bf16(128, 64 * kVGroup, 0, 1);
@@ -713,6 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit_warp(bar(B_MMAFIN));
       mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
       __syncwarp();
+      cluster_arrive_relaxed();   // the releases to the QK CTA precede MMAFIN
     } else if (warp >= 4) {
       // ---- row warps: rescale O rows on command, then the split's partial;
       // warpgroup `half` owns columns [256*half, 256*half + 256)
@@ -753,13 +763,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                        mbar_wait(bar(B_MMAFIN), 0, abort_flag, kWaitCycles);
       // all row warps agree before the staged write-out below
       const bool go = named_sync_and(kSoftmaxBar, kSoftmax, __all_sync(0xffffffffu, fin));
+      cluster_arrive_relaxed();   // FIN received: the QK CTA writes here no more
       if (go) {
         if (tid == 128) VA_TRACE_CTA(7, 5);
         tc_fence_after();
         // The split's partial (128 rows x 512, normalised by the row sum,
         // rounded to bf16) leaves through shared memory and the bulk-copy
-        // engine, one 1 KB row per copy: the P and value buffers are idle now
-        // and hold all 128 padded rows.
+        // engine, one 512-byte half row per copy: the P and value buffers are
+        // idle now and hold all 128 padded rows.
         const float inv = reinterpret_cast<const float*>(gb + kOffFin)[r];
         uint8_t* stg = gb + kOffP;
         uint8_t* rowp = stg + r * kEpiRowBytes + 512 * half;
@@ -780,22 +791,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(rowp + 64 * c + 16 * j) =
                 make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
-        fence_proxy_async_cta();   // staged rows, read by the bulk copies
+        fence_proxy_async_cta();   // staged half row, read by this thread's bulk copy
         if (tid == 128) VA_TRACE_CTA(5, 0);
-        named_sync(kSoftmaxBar, kSoftmax);
-        // warps 4-7 issue the row copies, one row per lane, and wait until
-        // they are written before the CTA retires
-        if (warp < 8) {
-          const int rr = (warp - 4) * 32 + lane;
-          const int lrr = row0 + rr;
-          if (lrr < R)
-            bulk_store_global(p.part_o + (size_t(split) * rows_total + size_t(b) * R + lrr) * kDv,
-                              smem_u32(stg + rr * kEpiRowBytes), uint32_t(kDv * 2));
-          bulk_commit();
-          bulk_wait<0>();
-          if (lane == 0 && warp == 4) VA_TRACE_CTA(5, 1);
-        }
-        named_sync(kSoftmaxBar, kSoftmax);
+        // each thread sends its own half row as soon as it is staged, and
+        // waits only until the copy has read it (the writes complete before
+        // the grid does)
+        if (row_ok)
+          bulk_store_global(p.part_o + (size_t(split) * rows_total + size_t(b) * R + lr) * kDv + 256 * half,
+                            smem_u32(rowp), 512u);
+        bulk_commit();
+        bulk_wait_read<0>();
+        if (lane == 0 && warp == 4) VA_TRACE_CTA(5, 1);
       } else if (ok && !fin) {
         fail();
       }
@@ -810,7 +816,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  cluster_sync();
+  // Neither CTA leaves while the other may still touch its shared memory.
+  // The PV CTA's threads arrived once they were done with the QK CTA: its
+  // producers after their last copy, its MMA warp after the last products
+  // (whose P-buffer releases reach the QK CTA, which waits for them itself),
+  // its row warps once the QK CTA's row sums had landed.  So the QK CTA
+  // leaves during the PV CTA's write-out, and the PV CTA, arrived already,
+  // only waits here for the QK CTA to have arrived.
+  if (rank == 0)
+    cluster_sync();
+  else
+    cluster_wait();
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 4);
 }
 
@@ -887,16 +903,30 @@ bool encode_pool_map(CUtensorMap* m, const Params& p, int blocks) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the queries: 3-D (64 features, query rows B*T*H, column
+// blocks: strides one 1152-byte row and 128 bytes); a box of 64 rows x 9
+// blocks is half a row block's Q.
+bool encode_q_map(CUtensorMap* m, const Params& p) {
+  cuuint64_t dims[3] = {64u, cuuint64_t(p.B) * cuuint64_t(p.rows_per_req), cuuint64_t(kKBlocks)};
+  cuuint64_t strides[2] = {cuuint64_t(kDqk) * 2u, 128u};
+  cuuint32_t box[3] = {64u, 64u, uint32_t(kKBlocks)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(p.q), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st) {
   // Contiguous pools are read with TMA box loads; the maps are encoded on the
   // host for this call's pool.  Paged calls do not use them.
-  CUtensorMap tk, tv, t2;
+  CUtensorMap tk, tv, t2, tq;
   memset(&tk, 0, sizeof tk);
   memset(&tv, 0, sizeof tv);
   memset(&t2, 0, sizeof t2);
+  if (!g_encode || !encode_q_map(&tq, p)) return cudaErrorNotSupported;
   int box3d = 0;
   if (p.kv_start) {
-    if (!g_encode || !encode_pool_map(&t2, p, 0)) return cudaErrorNotSupported;
+    if (!encode_pool_map(&t2, p, 0)) return cudaErrorNotSupported;
     if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) box3d = 1;
   }
   // launched with programmatic stream serialization: the clusters start
@@ -912,7 +942,7 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p, tk, tv, t2, box3d);
+  return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p, tk, tv, t2, tq, box3d);
 }
 
 }  // namespace va
