@@ -67,6 +67,8 @@ typedef struct CUstream_st *va_stream_t;
                                        request's prefix is clamped to what exists  */
 #define VA_STATUS_TIMEOUT     0x8u  /* a bounded device-side wait gave up            */
 #define VA_STATUS_BAD_DST     0x10u /* defrag destination outside the pool           */
+#define VA_STATUS_BAD_MASK    0x20u /* a dense mask row past custom_mask_len; the
+                                       node's missing draft columns read as 0      */
 
 /* Fixed widths of the MLA latent row. */
 #define VA_D_QK 576   /* key / query width: 512 latent + 64 rotary */
@@ -167,6 +169,41 @@ int verify_attn_contiguous(const void *q, const void *kv_pool, int64_t num_slots
                            const uint64_t *tree_bits, int B, int T, int H, float sm_scale,
                            int nsplit, int flags, void *workspace, size_t workspace_bytes,
                            void *out, float *lse, va_stream_t stream);
+
+/*
+ * Segmented verify attention: the prefix and the draft nodes' keys come as two
+ * slot lists, and the tree may come as a dense mask (The Checkpoint Report,
+ * "Mistakes and Incorrect Assumptions": the extend call takes the prefix in
+ * kv_indices and the draft tokens' own keys at out_cache_loc, and its custom
+ * mask holds one row per draft token with stride prefix + q_len).  Computes
+ * exactly what verify_attn_paged computes on the concatenated list.
+ *   kv_indices     int32 device; request b's prefix slots are
+ *                  kv_indices[kv_indptr[b] .. kv_indptr[b+1]), so its prefix
+ *                  length is P_b = kv_indptr[b+1] - kv_indptr[b] (no
+ *                  prefix_len argument).
+ *   kv_indptr      int32 [B+1] device, non-decreasing.
+ *   out_cache_loc  int32 [B*T] device; out_cache_loc[b*T + i] is the slot of
+ *                  request b's draft node i.
+ *   custom_mask    uint8 device (0 = hidden, non-zero = visible), or NULL.
+ *                  Request b's T rows of P_b + T entries each start at entry
+ *                  T * (kv_indptr[b] - kv_indptr[0] + b*T); row i, column
+ *                  P_b + k says whether node i sees draft node k.  Only those
+ *                  last T columns are read: every prefix key is visible to
+ *                  every draft node.  Entries at or past custom_mask_len are
+ *                  read as 0 and flag VA_STATUS_BAD_MASK.
+ *   custom_mask_len entries in custom_mask (ignored when it is NULL).
+ *   tree_parent, tree_bits  as for verify_attn_paged; exactly one of
+ *                  custom_mask, tree_bits, tree_parent is used, in that order
+ *                  of precedence.
+ * Every other argument is as for verify_attn_paged.
+ */
+int verify_attn_segmented(const void *q, const void *kv_pool, int64_t num_slots,
+                          int64_t kv_row_stride, const int32_t *kv_indices,
+                          const int32_t *kv_indptr, const int32_t *out_cache_loc,
+                          const uint8_t *custom_mask, int64_t custom_mask_len,
+                          const int32_t *tree_parent, const uint64_t *tree_bits, int B, int T,
+                          int H, float sm_scale, int nsplit, int flags, void *workspace,
+                          size_t workspace_bytes, void *out, float *lse, va_stream_t stream);
 
 /*
  * KV defragmentation (The Checkpoint Report, "Input Knowledge Required" and

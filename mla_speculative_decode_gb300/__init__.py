@@ -31,6 +31,7 @@ STATUS_BAD_PARENT = 0x2
 STATUS_BAD_INDPTR = 0x4
 STATUS_TIMEOUT = 0x8
 STATUS_BAD_DST = 0x10
+STATUS_BAD_MASK = 0x20
 PATH_AUTO, PATH_FMA, PATH_TC = 0, 1, 2
 
 LIB_PATH = _build_mod.LIB
@@ -75,6 +76,9 @@ def load() -> ctypes.CDLL:
     lib.verify_attn_contiguous.argtypes = [P, P, i64, i64, P, P, P, P, i32, i32, i32, f32, i32, i32,
                                            P, sz, P, P, P]
     lib.verify_attn_contiguous.restype = i32
+    lib.verify_attn_segmented.argtypes = [P, P, i64, i64, P, P, P, P, i64, P, P, i32, i32, i32,
+                                          f32, i32, i32, P, sz, P, P, P]
+    lib.verify_attn_segmented.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
     lib.verify_attn_paged_noalloc.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32,
@@ -223,6 +227,51 @@ def verify_attn_contiguous(q: torch.Tensor, kv_pool: torch.Tensor, kv_start: tor
         _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags, _ptr(workspace),
         workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
     _check("verify_attn_contiguous", rc)
+    return out, lse
+
+
+def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: torch.Tensor,
+                          kv_indptr: torch.Tensor, out_cache_loc: torch.Tensor,
+                          custom_mask: Optional[torch.Tensor] = None,
+                          tree_parent: Optional[torch.Tensor] = None,
+                          tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                          nsplit: int = 0, flags: int = PATH_AUTO,
+                          workspace: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Two-list variant: request b's prefix slots are kv_indices[kv_indptr[b]:kv_indptr[b+1]]
+    (int32), its draft nodes' slots out_cache_loc[b*T:(b+1)*T] (int32 [B*T]); the tree is a
+    dense extend mask (uint8 or bool, rows of prefix + T entries, only the last T read), or
+    tree_parent / tree_bits as for verify_attn_paged."""
+    init(q.device.index)
+    _dev(q, "q", torch.bfloat16)
+    _dev(kv_pool, "kv_pool", torch.bfloat16)
+    _dev(kv_indices, "kv_indices", torch.int32)
+    _dev(kv_indptr, "kv_indptr", torch.int32)
+    _dev(out_cache_loc, "out_cache_loc", torch.int32)
+    if q.dim() != 3 or q.shape[2] != D_QK or kv_pool.dim() != 2:
+        raise ValueError("q must be [B*T, H, 576] and kv_pool [num_slots, stride]")
+    B = kv_indptr.shape[0] - 1
+    T = q.shape[0] // B
+    H = q.shape[1]
+    if out_cache_loc.numel() != B * T:
+        raise ValueError("out_cache_loc must hold B*T slots")
+    mask_ptr, mask_len = None, 0
+    if custom_mask is not None:
+        if custom_mask.dtype == torch.bool:
+            custom_mask = custom_mask.view(torch.uint8)
+        _dev(custom_mask, "custom_mask", torch.uint8)
+        mask_ptr, mask_len = _ptr(custom_mask), custom_mask.numel()
+    if workspace is None:
+        workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
+    out, lse = _outputs(q.shape[0], H, q.device, out, lse)
+    par, bits = _tree_args(tree_parent, tree_bits)
+    rc = load().verify_attn_segmented(
+        _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_indices),
+        _ptr(kv_indptr), _ptr(out_cache_loc), mask_ptr, mask_len, par, bits, B, T, H,
+        float(sm_scale), nsplit, flags, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+        _stream(stream))
+    _check("verify_attn_segmented", rc)
     return out, lse
 
 

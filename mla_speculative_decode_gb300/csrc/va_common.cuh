@@ -50,10 +50,13 @@ struct Params {
   const __nv_bfloat16* kv;     // [num_slots, kv_stride]
   int64_t num_slots;
   int64_t kv_stride;           // elements
-  const int32_t* slot_idx;     // paged: concatenated slot lists
-  const int32_t* kv_indptr;    // paged: [B+1]
+  const int32_t* slot_idx;     // paged: concatenated slot lists; segmented: prefix lists
+  const int32_t* kv_indptr;    // paged, segmented: [B+1]
   const int64_t* kv_start;     // contiguous: [B] (NULL when paged)
-  const int32_t* prefix_len;   // [B]
+  const int32_t* draft_slots;  // segmented: [B*T] slots of the draft nodes (else NULL)
+  const int32_t* prefix_len;   // [B] (NULL when segmented: the prefix list's length)
+  const uint8_t* dense_mask;   // segmented: dense extend mask rows, or NULL
+  int64_t dense_mask_len;      // entries in dense_mask
   const int32_t* tree_parent;  // [B, T] or NULL
   const uint64_t* bits;        // [B, T] ancestor-or-self masks (caller's or workspace)
   int B, T, H;
@@ -91,16 +94,32 @@ __host__ __device__ inline SplitRange split_range(int N, int nsplit, int s) {
 
 // Per-request key bookkeeping read on the device.
 struct ReqInfo {
-  int P;        // effective prefix length
-  int N;        // P + T
-  int nlist;    // keys that have a slot (paged: slot list length; contiguous: N)
-  int64_t base; // paged: offset into slot_idx; contiguous: first pool row
+  int P;         // effective prefix length
+  int N;         // P + T
+  int nlist;     // keys that have a slot (paged: slot list length; contiguous: N)
+  int64_t base;  // paged, segmented: offset into slot_idx; contiguous: first pool row
+  int64_t dbase; // segmented: draft key j >= P is draft_slots[dbase + j]
 };
 
 __device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
   ReqInfo r;
-  int P = p.prefix_len[b];
+  r.dbase = 0;
   bool bad = false;
+  if (p.draft_slots) {
+    // segmented: the prefix is the whole prefix list, the draft nodes' slots
+    // are a list of their own
+    const int i0 = p.kv_indptr[b], i1 = p.kv_indptr[b + 1];
+    int P = i1 - i0;
+    if (P < 0) { P = 0; bad = true; }
+    r.P = P;
+    r.N = P + p.T;
+    r.nlist = r.N;
+    r.base = i0;
+    r.dbase = int64_t(b) * p.T - P;
+    if (bad && flag) atomicOr(p.status, VA_STATUS_BAD_INDPTR);
+    return r;
+  }
+  int P = p.prefix_len[b];
   if (P < 0) { P = 0; bad = true; }
   if (p.kv_start == nullptr) {
     int i0 = p.kv_indptr[b], i1 = p.kv_indptr[b + 1];
@@ -125,7 +144,9 @@ __device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
 // Pool row of key j of a request, or -1 when the key has no valid row.
 __device__ inline int64_t key_row(const Params& p, const ReqInfo& r, int j) {
   if (j >= r.nlist) return -1;
-  int64_t s = p.kv_start ? r.base + j : int64_t(p.slot_idx[r.base + j]);
+  int64_t s = p.kv_start ? r.base + j
+              : (p.draft_slots && j >= r.P) ? int64_t(p.draft_slots[r.dbase + j])
+                                             : int64_t(p.slot_idx[r.base + j]);
   return (s >= 0 && s < p.num_slots) ? s : -1;
 }
 

@@ -66,15 +66,23 @@ int pick_path(int flags, int B, int T, int H) {
   return va::tc_supported(B, T, H) ? VA_PATH_TC : VA_PATH_FMA;
 }
 
+// Shared by the entry points.  Key addressing: kv_start (contiguous rows),
+// else slot_idx + indptr (paged), with draft_slots the draft nodes' own list
+// (segmented; prefix lengths then come from indptr and prefix_len is NULL).
+// Tree: dense_mask, else bits, else parent.
 int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stride,
                   const int32_t* slot_idx, const int32_t* indptr, const int64_t* kv_start,
-                  const int32_t* prefix_len, const int32_t* parent, const uint64_t* bits, int B,
+                  const int32_t* draft_slots, const int32_t* prefix_len, const uint8_t* dense_mask,
+                  int64_t dense_mask_len, const int32_t* parent, const uint64_t* bits, int B,
                   int T, int H, float sm_scale, int nsplit, int flags, void* ws, size_t ws_bytes,
                   void* out, float* lse, cudaStream_t st) {
   const bool paged = kv_start == nullptr;
-  if (!q || !kv || !prefix_len || !ws || !out || !lse) return VA_ERR_NULL;
+  const bool segmented = draft_slots != nullptr;
+  if (!q || !kv || !ws || !out || !lse) return VA_ERR_NULL;
+  if (!segmented && !prefix_len) return VA_ERR_NULL;
   if (paged && (!slot_idx || !indptr)) return VA_ERR_NULL;
-  if (!parent && !bits) return VA_ERR_NULL;
+  if (!parent && !bits && !dense_mask) return VA_ERR_NULL;
+  if (dense_mask && dense_mask_len < 0) return VA_ERR_SHAPE;
   if (B < 1 || B > 65535 || T < 1 || T > VA_T_MAX || H < 1) return VA_ERR_SHAPE;
   if (int64_t(B) * T * H > (int64_t(1) << 24)) return VA_ERR_SHAPE;
   if (num_slots < 1 || stride < VA_D_QK) return VA_ERR_SHAPE;
@@ -83,7 +91,8 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   if (!isfinite(sm_scale)) return VA_ERR_SHAPE;
   if (stride % 8 != 0) return VA_ERR_ALIGN;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(ws, 256) ||
-      !aligned(lse, 4) || !aligned(prefix_len, 4))
+      !aligned(lse, 4) || (prefix_len && !aligned(prefix_len, 4)) ||
+      (draft_slots && !aligned(draft_slots, 4)))
     return VA_ERR_ALIGN;
   if ((slot_idx && !aligned(slot_idx, 4)) || (indptr && !aligned(indptr, 4)) ||
       (parent && !aligned(parent, 4)) || (bits && !aligned(bits, 8)) ||
@@ -115,9 +124,12 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   p.slot_idx = paged ? slot_idx : nullptr;
   p.kv_indptr = paged ? indptr : nullptr;
   p.kv_start = kv_start;
-  p.prefix_len = prefix_len;
-  p.tree_parent = bits ? nullptr : parent;
-  p.bits = bits ? bits : reinterpret_cast<const uint64_t*>(w + L.bits);
+  p.draft_slots = draft_slots;
+  p.prefix_len = segmented ? nullptr : prefix_len;
+  p.dense_mask = dense_mask;
+  p.dense_mask_len = dense_mask ? dense_mask_len : 0;
+  p.tree_parent = (bits || dense_mask) ? nullptr : parent;
+  p.bits = (bits && !dense_mask) ? bits : reinterpret_cast<const uint64_t*>(w + L.bits);
   p.B = B;
   p.T = T;
   p.H = H;
@@ -197,9 +209,10 @@ VA_API int verify_attn_paged(const void* q, const void* kv_pool, int64_t num_slo
                              int H, float sm_scale, int nsplit, int flags, void* workspace,
                              size_t workspace_bytes, void* out, float* lse, va_stream_t stream) {
   if (!slot_idx || !kv_indptr) return VA_ERR_NULL;
-  return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr,
-                       prefix_len, tree_parent, tree_bits, B, T, H, sm_scale, nsplit, flags,
-                       workspace, workspace_bytes, out, lse, reinterpret_cast<cudaStream_t>(stream));
+  return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr, nullptr,
+                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, nsplit,
+                       flags, workspace, workspace_bytes, out, lse,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_API int verify_attn_contiguous(const void* q, const void* kv_pool, int64_t num_slots,
@@ -209,9 +222,25 @@ VA_API int verify_attn_contiguous(const void* q, const void* kv_pool, int64_t nu
                                   int nsplit, int flags, void* workspace, size_t workspace_bytes,
                                   void* out, float* lse, va_stream_t stream) {
   if (!kv_start) return VA_ERR_NULL;
-  return verify_common(q, kv_pool, num_slots, kv_row_stride, nullptr, nullptr, kv_start,
-                       prefix_len, tree_parent, tree_bits, B, T, H, sm_scale, nsplit, flags,
-                       workspace, workspace_bytes, out, lse, reinterpret_cast<cudaStream_t>(stream));
+  return verify_common(q, kv_pool, num_slots, kv_row_stride, nullptr, nullptr, kv_start, nullptr,
+                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, nsplit,
+                       flags, workspace, workspace_bytes, out, lse,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+VA_API int verify_attn_segmented(const void* q, const void* kv_pool, int64_t num_slots,
+                                 int64_t kv_row_stride, const int32_t* kv_indices,
+                                 const int32_t* kv_indptr, const int32_t* out_cache_loc,
+                                 const uint8_t* custom_mask, int64_t custom_mask_len,
+                                 const int32_t* tree_parent, const uint64_t* tree_bits, int B,
+                                 int T, int H, float sm_scale, int nsplit, int flags,
+                                 void* workspace, size_t workspace_bytes, void* out, float* lse,
+                                 va_stream_t stream) {
+  if (!kv_indices || !kv_indptr || !out_cache_loc) return VA_ERR_NULL;
+  return verify_common(q, kv_pool, num_slots, kv_row_stride, kv_indices, kv_indptr, nullptr,
+                       out_cache_loc, nullptr, custom_mask, custom_mask_len, tree_parent,
+                       tree_bits, B, T, H, sm_scale, nsplit, flags, workspace, workspace_bytes,
+                       out, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_API int verify_attn_defrag(void* kv_pool, int64_t num_slots, int64_t kv_row_stride,
@@ -268,9 +297,10 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
     while (ns > 1 && va::ws_layout(B, T, H, ns).total > cap) --ns;
   }
   if (va::ws_layout(B, T, H, ns).total > cap) return VA_ERR_WORKSPACE;
-  return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr,
-                       prefix_len, tree_parent, tree_bits, B, T, H, sm_scale, ns, flags,
-                       g_noalloc_ptr[dev], cap, out, lse, reinterpret_cast<cudaStream_t>(stream));
+  return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr, nullptr,
+                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, ns,
+                       flags, g_noalloc_ptr[dev], cap, out, lse,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_API int va_set_partial_events(void* before, void* after) {

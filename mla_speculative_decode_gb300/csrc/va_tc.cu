@@ -163,15 +163,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sum) {
 }
 
 // Raw pool row of key j of the split as stored in the slot list (contiguous
-// pools: the row itself), or -1 when j is past the split or the list.  The
-// value is only range-checked when it is used, a tile later, so the load's
-// latency overlaps the current tile's copies instead of stalling the warp.
+// pools: the row itself; segmented lists: the draft list past the prefix), or
+// -1 when j is past the split or the list.  The value is only range-checked
+// when it is used, a tile later, so the load's latency overlaps the current
+// tile's copies instead of stalling the warp.
 __device__ __forceinline__ int fetch_row(const Params& p, const ReqInfo& ri, int j, int k1) {
   if (j >= k1 || j >= ri.nlist) return -1;
   if (p.kv_start) {
     const int64_t r = ri.base + j;
     return (r >= 0 && r < p.num_slots && r <= 0x7fffffff) ? int(r) : -1;
   }
+  if (p.draft_slots && j >= ri.P) return __ldg(p.draft_slots + ri.dbase + j);
   return __ldg(p.slot_idx + ri.base + j);
 }
 // A fetched row, or -1 (no row: the copy zero-fills) when out of the pool.

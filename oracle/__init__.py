@@ -22,6 +22,11 @@ Functions and the passages they follow (page titles and sections):
                    "The Deeper Significance" (reduction kernel).
   defrag        -- The Checkpoint Report, "Input Knowledge Required" (KV
                    defragmentation keeps per-request KV contiguous).
+  segmented_lists, dense_mask_bits
+                -- The Checkpoint Report, "Mistakes and Incorrect Assumptions"
+                   (the extend call takes the prefix slots in kv_indices, the
+                   draft tokens' own slots at out_cache_loc, and a custom mask
+                   with one row per draft token of stride prefix + q_len).
 """
 from __future__ import annotations
 
@@ -168,6 +173,58 @@ def lse_merge(lse_parts, o_parts):
         out[r] = o1
         lse[r] = l1[0]
     return out, lse
+
+
+def segmented_lists(kv_indices, kv_indptr, out_cache_loc, T: int):
+    """Two slot lists -> one list per request, prefix first, then the draft nodes.
+
+    Request b's prefix slots are kv_indices[kv_indptr[b]:kv_indptr[b+1]] and its
+    draft nodes' slots out_cache_loc[b*T:(b+1)*T].  Returns (slots int32,
+    indptr int64 [B+1], prefix_len int32 [B]) in the layout ``verify_attn`` takes.
+    """
+    ind = [int(x) for x in np.asarray(kv_indices).reshape(-1)]
+    ip = [int(x) for x in np.asarray(kv_indptr).reshape(-1)]
+    loc = [int(x) for x in np.asarray(out_cache_loc).reshape(-1)]
+    B = len(ip) - 1
+    slots, indptr, prefix = [], [0], []
+    for b in range(B):
+        pre = ind[ip[b]:ip[b + 1]]
+        slots += pre + loc[b * T:(b + 1) * T]
+        indptr.append(len(slots))
+        prefix.append(len(pre))
+    return (np.array(slots, dtype=np.int32), np.array(indptr, dtype=np.int64),
+            np.array(prefix, dtype=np.int32))
+
+
+def dense_mask_bits(custom_mask, kv_indptr, T: int):
+    """Dense extend-mask rows -> the draft-key part of each node's visible set.
+
+    Request b (prefix P_b = kv_indptr[b+1] - kv_indptr[b]) owns T rows of P_b + T
+    entries, after the rows of the requests before it; bit k of node i's set is
+    row i, column P_b + k (non-zero = visible).  Entries past the end of the mask
+    count as 0.  Returns (bits uint64 [B, T], number of entries past the end).
+    """
+    m = np.asarray(custom_mask).reshape(-1)
+    ip = [int(x) for x in np.asarray(kv_indptr).reshape(-1)]
+    B = len(ip) - 1
+    bits = np.zeros((B, T), dtype=np.uint64)
+    missing = 0
+    start = 0                      # first entry of request b's rows
+    for b in range(B):
+        P = max(ip[b + 1] - ip[b], 0)
+        for i in range(T):
+            row = start + i * (P + T)
+            v = 0
+            for k in range(T):
+                e = row + P + k
+                if 0 <= e < m.shape[0]:
+                    if m[e]:
+                        v |= 1 << k
+                else:
+                    missing += 1
+            bits[b, i] = v
+        start += T * (P + T)
+    return bits, missing
 
 
 def defrag(pool_bits, src_slots, src_indptr, dst_base):

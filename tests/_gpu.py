@@ -53,7 +53,8 @@ def compare(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out, ref_lse, rows
         o, l = o[rows], l[rows]
     err = np.abs(o - ref_out)
     assert np.all(np.isfinite(o)), "non-finite output"
-    lerr = np.abs(l - ref_lse)
+    with np.errstate(invalid="ignore"):     # -inf - -inf, handled just below
+        lerr = np.abs(l - ref_lse)
     same_inf = (np.isinf(l) & np.isinf(ref_lse) & (np.sign(l) == np.sign(ref_lse)))
     lerr = np.where(same_inf, 0.0, lerr)
     stats = dict(max_abs=float(err.max()), mean_abs=float(err.mean()), lse_max=float(lerr.max()))

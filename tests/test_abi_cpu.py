@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    for n in ("verify_attn_paged", "verify_attn_contiguous", "verify_attn_defrag",
+    for n in ("verify_attn_paged", "verify_attn_contiguous", "verify_attn_segmented",
+              "verify_attn_defrag",
               "va_workspace_bytes", "va_init", "va_read_status", "va_auto_nsplit", "va_version",
               "va_set_partial_events"):
         assert n in names
@@ -110,6 +111,32 @@ def test_contiguous_argument_errors(lib):
     assert f(*bad) == -3
     bad = list(base); bad[15] = 10
     assert f(*bad) == -4
+
+
+def _segmented(lib, **over):
+    a = dict(q=A16, kv=A16, num_slots=4096, stride=576, indices=A16, indptr=A16, loc=A16,
+             mask=A16, mask_len=1000, parent=None, bits=None, B=1, T=4, H=8, scale=0.07, nsplit=4,
+             flags=0, ws=A256, ws_bytes=1 << 30, out=A16, lse=A16, stream=None)
+    a.update(over)
+    return lib.verify_attn_segmented(a["q"], a["kv"], a["num_slots"], a["stride"], a["indices"],
+                                     a["indptr"], a["loc"], a["mask"], a["mask_len"], a["parent"],
+                                     a["bits"], a["B"], a["T"], a["H"], a["scale"], a["nsplit"],
+                                     a["flags"], a["ws"], a["ws_bytes"], a["out"], a["lse"],
+                                     a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(indices=None), -1), (dict(indptr=None), -1), (dict(loc=None), -1), (dict(q=None), -1),
+    (dict(mask=None), -1), (dict(mask_len=-1), -2), (dict(T=65), -2), (dict(loc=A16 + 2), -3),
+    (dict(indices=A16 + 2), -3), (dict(ws_bytes=1000), -4),
+])
+def test_segmented_argument_errors(lib, over, code):
+    assert _segmented(lib, **over) == code
+
+
+def test_segmented_valid_arguments_without_gpu_do_not_crash(lib):
+    assert _segmented(lib) in (-5, -7)
+    assert _segmented(lib, mask=None, parent=A16) in (-5, -7)
 
 
 def test_defrag_argument_errors(lib):

@@ -136,6 +136,91 @@ def test_extend_mask_golden_through_attention(oracle_mod):
         assert abs(lse[i] - math.log(vis.sum())) < 1e-15
 
 
+def test_segmented_lists_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "segmented_small.txt"))
+    T = int(g["T"])
+    ints = lambda k: [int(x) for x in g[k].split()]
+    slots, indptr, prefix = oracle_mod.segmented_lists(ints("kv_indices"), ints("kv_indptr"),
+                                                       ints("out_cache_loc"), T)
+    assert slots.tolist() == ints("slots")
+    assert indptr.tolist() == ints("indptr")
+    assert prefix.tolist() == ints("prefix")
+
+
+def test_dense_mask_bits_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "segmented_small.txt"))
+    T = int(g["T"])
+    mask = np.array([int(x) for x in g["mask"].split()], dtype=np.uint8)
+    bits, missing = oracle_mod.dense_mask_bits(mask, [int(x) for x in g["kv_indptr"].split()], T)
+    assert missing == 0
+    assert bits.reshape(-1).tolist() == [int(x) for x in g["bits"].split()]
+
+
+def test_dense_mask_bits_of_the_extend_mask_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "extend_mask_small.txt"))
+    P = int(g["prefix"])
+    parent = [int(x) for x in g["parent"].split()]
+    T = len(parent)
+    mask = np.concatenate([np.array([int(x) for x in g[f"row{i}"].split()]) for i in range(T)])
+    bits, missing = oracle_mod.dense_mask_bits(mask, [0, P], T)
+    want, _ = oracle_mod.tree_bits(np.array(parent, dtype=np.int32)[None])
+    assert missing == 0 and bits.tolist() == want.tolist()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_dense_mask_bits_vs_tree_bits(oracle_mod, seed):
+    """Masks from the transitive closure of the parent relation, read back as
+    bits, equal the parent walk's sets; requests of different prefix lengths
+    (one empty) place their rows one after the other."""
+    rng = np.random.default_rng(seed)
+    B, T = 4, 9
+    prefixes = [0, 5, 1, 12]
+    parents = np.array([[rng.integers(-1, i) for i in range(T)] for _ in range(B)], dtype=np.int32)
+    flat = np.concatenate([_dense_mask(parents[b], prefixes[b]).reshape(-1) for b in range(B)])
+    indptr = np.concatenate([[3], 3 + np.cumsum(prefixes)])   # non-zero start
+    bits, missing = oracle_mod.dense_mask_bits(flat.astype(np.uint8), indptr, T)
+    want, bad = oracle_mod.tree_bits(parents)
+    assert missing == 0 and bad == 0
+    assert bits.tolist() == want.tolist()
+
+
+def test_dense_mask_bits_short_mask_reads_zero(oracle_mod):
+    mask = np.ones(2 * (3 + 2), dtype=np.uint8)            # T=2 rows of prefix 3 + 2
+    bits, missing = oracle_mod.dense_mask_bits(mask[:-1], [0, 3], 2)
+    assert missing == 1 and bits.tolist() == [[3, 1]]
+
+
+def test_segmented_attention_is_slot_relocation_invariant(oracle_mod):
+    """Draft rows moved to other pool slots, with out_cache_loc following them,
+    give bit-identical attention."""
+    w = _tiny(B=2, H=2, T=3, prefix=(4, 0), num_slots=64, seed=5)
+    sl, ip = w.slot_idx.numpy(), w.kv_indptr.numpy()
+    P = w.prefix_len.numpy()
+    T = w.spec.T
+    ind = np.concatenate([sl[ip[b]:ip[b] + P[b]] for b in range(2)])
+    kip = np.concatenate([[0], np.cumsum(P)])
+    loc = np.concatenate([sl[ip[b] + P[b]:ip[b + 1]] for b in range(2)])
+    bits, _ = oracle_mod.tree_bits(w.parents.numpy())
+
+    def attn(kv, loc_):
+        s2, ip2, p2 = oracle_mod.segmented_lists(ind, kip, loc_, T)
+        return oracle_mod.verify_attn(synth.as_u16(w.q), synth.as_u16(kv), s2, ip2, p2, bits,
+                                      w.spec.sm_scale)[:2]
+
+    o1, l1 = attn(w.kv_pool, loc)
+    used = set(sl.tolist())
+    free = [r for r in range(w.kv_pool.shape[0]) if r not in used][:len(loc)]
+    kv2 = w.kv_pool.clone()
+    for a, b2 in zip(loc, free):
+        kv2[b2] = w.kv_pool[a]
+        kv2[a] = 0
+    o2, l2 = attn(kv2, np.array(free, dtype=np.int32))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    o0, l0 = oracle_mod.verify_attn(synth.as_u16(w.q), synth.as_u16(w.kv_pool), sl, ip, P, bits,
+                                    w.spec.sm_scale)[:2]
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
 # ------------------------------------------------------ brute force / library
 
 @pytest.mark.parametrize("seed,H,T,P,tree", [(1, 2, 3, 4, "random"), (2, 1, 4, 0, "random"),
