@@ -231,7 +231,7 @@ class Step:
         self.ws, self.nsplit = va.alloc_workspace(B, T, H, nsplit, path, dev)
         self.out = torch.empty(B * T, H, synth.D_V, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(B * T, H, dtype=torch.float32, device=dev)
-        if layout == "segmented":
+        if layout in ("segmented", "segmented_append"):
             # the extend call's two lists: prefix slots (kv_indices) and the
             # draft nodes' slots (out_cache_loc), and its dense mask rows
             # (prefix columns visible, draft columns the node's ancestors and
@@ -257,15 +257,19 @@ class Step:
                         k = par[b][k] if par[b][k] < k else -1
                     rows.append(r)
             self.mask = torch.from_numpy(np.concatenate(rows)).to(dev)
+            # the draft tokens' new latents, written into their slots by the call
+            self.draft = ((torch.randn(B * T, synth.D_QK, generator=g)).to(torch.bfloat16).to(dev)
+                          if layout == "segmented_append" else None)
         self.kv_bytes = self.N * synth.D_QK * 2
         # tensor-core work: 2176 flop (2*576 + 2*512) for every row and every key
         self.flops = sum(2176.0 * T * H * n for n in Ns)
 
     def call(self, k, stream=None):
-        if self.layout == "segmented":
+        if self.layout in ("segmented", "segmented_append"):
             self.va.verify_attn_segmented(self.q, self.pool, self.seg_ind[k % self.nrot],
                                           self.seg_indptr, self.seg_loc[k % self.nrot],
-                                          custom_mask=self.mask, sm_scale=synth.SM_SCALE,
+                                          custom_mask=self.mask, draft_kv=self.draft,
+                                          sm_scale=synth.SM_SCALE,
                                           nsplit=self.nsplit, flags=self.path, workspace=self.ws,
                                           out=self.out, lse=self.lse, stream=stream)
             return
@@ -653,14 +657,15 @@ def main():
         # segmented call (two slot lists + dense extend mask) on the TP8 slice,
         # beside the paged call on the same slots
         seg = {}
-        for lay in ("segmented", "scattered"):
+        for lay in ("segmented", "segmented_append", "scattered"):
             st = Step(va, pool, 8, 16, 4096, seed=1, nrot=16, dev=dev, path=args.path, nsplit=0,
                       layout=lay)
             med, p10, p90, k_us = measure_dist(st, 64, 8)
             seg[lay] = {"us_per_step": med, "p10": p10, "p90": p90,
                         "gbs": st.kv_bytes / (med * 1e-6) / 1e9, "partial_kernel_us": k_us}
             del st
-        configs["segmented TP8 H=8 T=16 P=4096 (kv_indices + out_cache_loc + dense mask) vs paged"] = seg
+        configs["segmented TP8 H=8 T=16 P=4096 (kv_indices + out_cache_loc + dense mask; "
+                "with the draft rows appended in the call) vs paged"] = seg
         torch.cuda.empty_cache()
         # defrag: 65536 scattered rows (lower half of the pool) compacted into a
         # contiguous range in the upper half

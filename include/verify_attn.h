@@ -184,6 +184,13 @@ int verify_attn_contiguous(const void *q, const void *kv_pool, int64_t num_slots
  *   kv_indptr      int32 [B+1] device, non-decreasing.
  *   out_cache_loc  int32 [B*T] device; out_cache_loc[b*T + i] is the slot of
  *                  request b's draft node i.
+ *   draft_kv       bf16 [B*T, 576] device (contiguous rows, 16-byte aligned),
+ *                  or NULL.  When given, the call first writes row b*T + i
+ *                  into the first 576 columns of pool row out_cache_loc[b*T +
+ *                  i] (the draft tokens' new latents), then verifies against
+ *                  the pool with those rows in place.  The draft slots must be
+ *                  distinct and must not hold any request's prefix key; a slot
+ *                  outside the pool is skipped (and flagged when read).
  *   custom_mask    uint8 device (0 = hidden, non-zero = visible), or NULL.
  *                  Request b's T rows of P_b + T entries each start at entry
  *                  T * (kv_indptr[b] - kv_indptr[0] + b*T); row i, column
@@ -200,7 +207,8 @@ int verify_attn_contiguous(const void *q, const void *kv_pool, int64_t num_slots
 int verify_attn_segmented(const void *q, const void *kv_pool, int64_t num_slots,
                           int64_t kv_row_stride, const int32_t *kv_indices,
                           const int32_t *kv_indptr, const int32_t *out_cache_loc,
-                          const uint8_t *custom_mask, int64_t custom_mask_len,
+                          const void *draft_kv, const uint8_t *custom_mask,
+                          int64_t custom_mask_len,
                           const int32_t *tree_parent, const uint64_t *tree_bits, int B, int T,
                           int H, float sm_scale, int nsplit, int flags, void *workspace,
                           size_t workspace_bytes, void *out, float *lse, va_stream_t stream);

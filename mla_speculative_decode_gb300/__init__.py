@@ -76,8 +76,8 @@ def load() -> ctypes.CDLL:
     lib.verify_attn_contiguous.argtypes = [P, P, i64, i64, P, P, P, P, i32, i32, i32, f32, i32, i32,
                                            P, sz, P, P, P]
     lib.verify_attn_contiguous.restype = i32
-    lib.verify_attn_segmented.argtypes = [P, P, i64, i64, P, P, P, P, i64, P, P, i32, i32, i32,
-                                          f32, i32, i32, P, sz, P, P, P]
+    lib.verify_attn_segmented.argtypes = [P, P, i64, i64, P, P, P, P, P, i64, P, P, i32, i32,
+                                          i32, f32, i32, i32, P, sz, P, P, P]
     lib.verify_attn_segmented.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
@@ -233,6 +233,7 @@ def verify_attn_contiguous(q: torch.Tensor, kv_pool: torch.Tensor, kv_start: tor
 def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: torch.Tensor,
                           kv_indptr: torch.Tensor, out_cache_loc: torch.Tensor,
                           custom_mask: Optional[torch.Tensor] = None,
+                          draft_kv: Optional[torch.Tensor] = None,
                           tree_parent: Optional[torch.Tensor] = None,
                           tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
                           nsplit: int = 0, flags: int = PATH_AUTO,
@@ -242,7 +243,8 @@ def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: to
     """Two-list variant: request b's prefix slots are kv_indices[kv_indptr[b]:kv_indptr[b+1]]
     (int32), its draft nodes' slots out_cache_loc[b*T:(b+1)*T] (int32 [B*T]); the tree is a
     dense extend mask (uint8 or bool, rows of prefix + T entries, only the last T read), or
-    tree_parent / tree_bits as for verify_attn_paged."""
+    tree_parent / tree_bits as for verify_attn_paged.  With draft_kv (bf16 [B*T, 576]) the
+    call first writes those rows into the pool at out_cache_loc."""
     init(q.device.index)
     _dev(q, "q", torch.bfloat16)
     _dev(kv_pool, "kv_pool", torch.bfloat16)
@@ -262,13 +264,18 @@ def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: to
             custom_mask = custom_mask.view(torch.uint8)
         _dev(custom_mask, "custom_mask", torch.uint8)
         mask_ptr, mask_len = _ptr(custom_mask), custom_mask.numel()
+    if draft_kv is not None:
+        _dev(draft_kv, "draft_kv", torch.bfloat16)
+        if tuple(draft_kv.shape) != (B * T, D_QK):
+            raise ValueError("draft_kv must be [B*T, 576]")
     if workspace is None:
         workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
     out, lse = _outputs(q.shape[0], H, q.device, out, lse)
     par, bits = _tree_args(tree_parent, tree_bits)
     rc = load().verify_attn_segmented(
         _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_indices),
-        _ptr(kv_indptr), _ptr(out_cache_loc), mask_ptr, mask_len, par, bits, B, T, H,
+        _ptr(kv_indptr), _ptr(out_cache_loc), _ptr(draft_kv), mask_ptr, mask_len, par, bits,
+        B, T, H,
         float(sm_scale), nsplit, flags, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
         _stream(stream))
     _check("verify_attn_segmented", rc)

@@ -54,6 +54,7 @@ struct Params {
   const int32_t* kv_indptr;    // paged, segmented: [B+1]
   const int64_t* kv_start;     // contiguous: [B] (NULL when paged)
   const int32_t* draft_slots;  // segmented: [B*T] slots of the draft nodes (else NULL)
+  const __nv_bfloat16* draft_kv;  // segmented: [B*T, 576] rows written to those slots first, or NULL
   const int32_t* prefix_len;   // [B] (NULL when segmented: the prefix list's length)
   const uint8_t* dense_mask;   // segmented: dense extend mask rows, or NULL
   int64_t dense_mask_len;      // entries in dense_mask

@@ -72,7 +72,8 @@ int pick_path(int flags, int B, int T, int H) {
 // Tree: dense_mask, else bits, else parent.
 int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stride,
                   const int32_t* slot_idx, const int32_t* indptr, const int64_t* kv_start,
-                  const int32_t* draft_slots, const int32_t* prefix_len, const uint8_t* dense_mask,
+                  const int32_t* draft_slots, const void* draft_kv, const int32_t* prefix_len,
+                  const uint8_t* dense_mask,
                   int64_t dense_mask_len, const int32_t* parent, const uint64_t* bits, int B,
                   int T, int H, float sm_scale, int nsplit, int flags, void* ws, size_t ws_bytes,
                   void* out, float* lse, cudaStream_t st) {
@@ -92,8 +93,9 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   if (stride % 8 != 0) return VA_ERR_ALIGN;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(ws, 256) ||
       !aligned(lse, 4) || (prefix_len && !aligned(prefix_len, 4)) ||
-      (draft_slots && !aligned(draft_slots, 4)))
+      (draft_slots && !aligned(draft_slots, 4)) || (draft_kv && !aligned(draft_kv, 16)))
     return VA_ERR_ALIGN;
+  if (draft_kv && !draft_slots) return VA_ERR_SHAPE;
   if ((slot_idx && !aligned(slot_idx, 4)) || (indptr && !aligned(indptr, 4)) ||
       (parent && !aligned(parent, 4)) || (bits && !aligned(bits, 8)) ||
       (kv_start && !aligned(kv_start, 8)))
@@ -125,6 +127,7 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   p.kv_indptr = paged ? indptr : nullptr;
   p.kv_start = kv_start;
   p.draft_slots = draft_slots;
+  p.draft_kv = static_cast<const __nv_bfloat16*>(draft_kv);
   p.prefix_len = segmented ? nullptr : prefix_len;
   p.dense_mask = dense_mask;
   p.dense_mask_len = dense_mask ? dense_mask_len : 0;
@@ -210,8 +213,8 @@ VA_API int verify_attn_paged(const void* q, const void* kv_pool, int64_t num_slo
                              size_t workspace_bytes, void* out, float* lse, va_stream_t stream) {
   if (!slot_idx || !kv_indptr) return VA_ERR_NULL;
   return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr, nullptr,
-                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, nsplit,
-                       flags, workspace, workspace_bytes, out, lse,
+                       nullptr, prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale,
+                       nsplit, flags, workspace, workspace_bytes, out, lse,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -223,22 +226,23 @@ VA_API int verify_attn_contiguous(const void* q, const void* kv_pool, int64_t nu
                                   void* out, float* lse, va_stream_t stream) {
   if (!kv_start) return VA_ERR_NULL;
   return verify_common(q, kv_pool, num_slots, kv_row_stride, nullptr, nullptr, kv_start, nullptr,
-                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, nsplit,
-                       flags, workspace, workspace_bytes, out, lse,
+                       nullptr, prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale,
+                       nsplit, flags, workspace, workspace_bytes, out, lse,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_API int verify_attn_segmented(const void* q, const void* kv_pool, int64_t num_slots,
                                  int64_t kv_row_stride, const int32_t* kv_indices,
                                  const int32_t* kv_indptr, const int32_t* out_cache_loc,
-                                 const uint8_t* custom_mask, int64_t custom_mask_len,
+                                 const void* draft_kv, const uint8_t* custom_mask,
+                                 int64_t custom_mask_len,
                                  const int32_t* tree_parent, const uint64_t* tree_bits, int B,
                                  int T, int H, float sm_scale, int nsplit, int flags,
                                  void* workspace, size_t workspace_bytes, void* out, float* lse,
                                  va_stream_t stream) {
   if (!kv_indices || !kv_indptr || !out_cache_loc) return VA_ERR_NULL;
   return verify_common(q, kv_pool, num_slots, kv_row_stride, kv_indices, kv_indptr, nullptr,
-                       out_cache_loc, nullptr, custom_mask, custom_mask_len, tree_parent,
+                       out_cache_loc, draft_kv, nullptr, custom_mask, custom_mask_len, tree_parent,
                        tree_bits, B, T, H, sm_scale, nsplit, flags, workspace, workspace_bytes,
                        out, lse, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -298,7 +302,7 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
   }
   if (va::ws_layout(B, T, H, ns).total > cap) return VA_ERR_WORKSPACE;
   return verify_common(q, kv_pool, num_slots, kv_row_stride, slot_idx, kv_indptr, nullptr, nullptr,
-                       prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, ns,
+                       nullptr, prefix_len, nullptr, 0, tree_parent, tree_bits, B, T, H, sm_scale, ns,
                        flags, g_noalloc_ptr[dev], cap, out, lse,
                        reinterpret_cast<cudaStream_t>(stream));
 }

@@ -22,9 +22,32 @@ namespace {
 
 constexpr int kWarps = 8;
 
+constexpr int kAppendRowsPerCta = 32;
+
 __global__ void __launch_bounds__(kWarps * 32) tree_bits_kernel(Params p, uint64_t* bits_out) {
   __shared__ int par[kWarps][kTmax];
   griddep_launch_dependents();   // the split-K kernel may start its set-up now
+  if (blockIdx.x > 0) {
+    // Draft-row append (segmented calls with draft_kv): row b*T + i of
+    // draft_kv goes to the pool row of request b's draft key P_b + i, one
+    // warp per row, 16-byte chunks.  Rows without a valid pool row are
+    // skipped (the split-K kernel flags them when it reads the key).  The
+    // split-K kernel reads draft keys only after griddepcontrol.wait, that
+    // is after this grid has completed.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = (blockIdx.x - 1) * kAppendRowsPerCta;
+    const int nrows = p.B * p.T;
+    for (int r = r0 + warp; r < r0 + kAppendRowsPerCta && r < nrows; r += kWarps) {
+      const int b = r / p.T, i = r - b * p.T;
+      const ReqInfo ri = req_info(p, b, false);
+      const int64_t row = key_row(p, ri, ri.P + i);
+      if (row < 0) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(p.draft_kv + size_t(r) * kDqk);
+      uint4* dst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(p.kv) + row * p.kv_stride);
+      for (int c = lane; c < kDqk / 8; c += 32) dst[c] = src[c];
+    }
+    return;
+  }
   if (threadIdx.x == 0) *p.status = 0u;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -84,7 +107,11 @@ __global__ void __launch_bounds__(kWarps * 32) tree_bits_kernel(Params p, uint64
 }  // namespace
 
 cudaError_t launch_tree_bits(const Params& p, uint64_t* bits_out, cudaStream_t st) {
-  tree_bits_kernel<<<1, kWarps * 32, 0, st>>>(p, bits_out);
+  // one CTA for the masks and the status word, and with draft rows to append,
+  // one more per kAppendRowsPerCta rows
+  const int rows = p.draft_kv ? p.B * p.T : 0;
+  const int grid = 1 + (rows + kAppendRowsPerCta - 1) / kAppendRowsPerCta;
+  tree_bits_kernel<<<grid, kWarps * 32, 0, st>>>(p, bits_out);
   return cudaGetLastError();
 }
 

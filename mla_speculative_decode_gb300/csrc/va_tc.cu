@@ -251,6 +251,9 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     const uint32_t fb = full0 + 8u * uint32_t(t & 1);
     // contiguous rows, whole tile inside the split and the pool: box loads
     const int tk0 = sr.k0 + t * kTile;
+    // a tile with draft keys, when the call appends their rows first: after
+    // the append (in the kernel before this one) has completed
+    if (p.draft_kv && tk0 + kTile > ri.P) griddep_wait();
     const int64_t row0 = p.kv_start ? ri.base + tk0 : -1;
     const bool boxes = p.kv_start != nullptr && tk0 + kTile <= sr.k1 && tk0 + kTile <= ri.nlist &&
                        row0 >= 0 && row0 + kTile <= p.num_slots && row0 + kTile <= 0x7fffffff;

@@ -22,11 +22,12 @@ Functions and the passages they follow (page titles and sections):
                    "The Deeper Significance" (reduction kernel).
   defrag        -- The Checkpoint Report, "Input Knowledge Required" (KV
                    defragmentation keeps per-request KV contiguous).
-  segmented_lists, dense_mask_bits
+  segmented_lists, dense_mask_bits, append_rows
                 -- The Checkpoint Report, "Mistakes and Incorrect Assumptions"
                    (the extend call takes the prefix slots in kv_indices, the
                    draft tokens' own slots at out_cache_loc, and a custom mask
-                   with one row per draft token of stride prefix + q_len).
+                   with one row per draft token of stride prefix + q_len;
+                   out_cache_loc is where the draft tokens' KV goes).
 """
 from __future__ import annotations
 
@@ -225,6 +226,17 @@ def dense_mask_bits(custom_mask, kv_indptr, T: int):
             bits[b, i] = v
         start += T * (P + T)
     return bits, missing
+
+
+def append_rows(pool_bits, rows_bits, slots):
+    """A copy of the pool with rows_bits[r] written into the first columns of
+    pool row slots[r] (slots outside the pool are skipped)."""
+    pool = np.array(pool_bits, dtype=np.uint16, copy=True, order="C")
+    rows = np.asarray(rows_bits, dtype=np.uint16)
+    for r, s in enumerate(np.asarray(slots).reshape(-1).tolist()):
+        if 0 <= s < pool.shape[0]:
+            pool[s, :rows.shape[1]] = rows[r]
+    return pool
 
 
 def defrag(pool_bits, src_slots, src_indptr, dst_base):

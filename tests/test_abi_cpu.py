@@ -115,11 +115,12 @@ def test_contiguous_argument_errors(lib):
 
 def _segmented(lib, **over):
     a = dict(q=A16, kv=A16, num_slots=4096, stride=576, indices=A16, indptr=A16, loc=A16,
-             mask=A16, mask_len=1000, parent=None, bits=None, B=1, T=4, H=8, scale=0.07, nsplit=4,
+             draft=None, mask=A16, mask_len=1000, parent=None, bits=None, B=1, T=4, H=8, scale=0.07, nsplit=4,
              flags=0, ws=A256, ws_bytes=1 << 30, out=A16, lse=A16, stream=None)
     a.update(over)
     return lib.verify_attn_segmented(a["q"], a["kv"], a["num_slots"], a["stride"], a["indices"],
-                                     a["indptr"], a["loc"], a["mask"], a["mask_len"], a["parent"],
+                                     a["indptr"], a["loc"], a["draft"], a["mask"], a["mask_len"],
+                                     a["parent"],
                                      a["bits"], a["B"], a["T"], a["H"], a["scale"], a["nsplit"],
                                      a["flags"], a["ws"], a["ws_bytes"], a["out"], a["lse"],
                                      a["stream"])
@@ -128,7 +129,7 @@ def _segmented(lib, **over):
 @pytest.mark.parametrize("over,code", [
     (dict(indices=None), -1), (dict(indptr=None), -1), (dict(loc=None), -1), (dict(q=None), -1),
     (dict(mask=None), -1), (dict(mask_len=-1), -2), (dict(T=65), -2), (dict(loc=A16 + 2), -3),
-    (dict(indices=A16 + 2), -3), (dict(ws_bytes=1000), -4),
+    (dict(indices=A16 + 2), -3), (dict(ws_bytes=1000), -4), (dict(draft=A16 + 8), -3),
 ])
 def test_segmented_argument_errors(lib, over, code):
     assert _segmented(lib, **over) == code

@@ -163,3 +163,90 @@ def test_segmented_status_clears_between_calls(va):
     assert va.read_status(ws) == va.STATUS_BAD_MASK
     _call(va, w, ind, kip, loc, mask=mask, ws=ws, ns=ns)
     assert va.read_status(ws) == 0
+
+
+# ------------------------------------------- draft rows appended in the call
+
+def _append_case(va, spec, path, stride=576):
+    spec.row_stride = stride
+    w = synth.make(spec)
+    ind, kip, loc = _split(w)
+    mask = _flat_mask(w)
+    g = torch.Generator().manual_seed(spec.seed + 1000)
+    draft = torch.randn(spec.B * spec.T, synth.D_QK, generator=g).to(torch.bfloat16)
+    # the draft slots hold NaN before the call: any read of them before the
+    # append shows in the output
+    w.kv_pool[torch.from_numpy(loc).long(), :synth.D_QK] = float("nan")
+    pool0 = w.kv_pool.clone()
+    kv_dev = w.kv_pool.cuda()
+    ws, ns = va.alloc_workspace(spec.B, spec.T, spec.H, 0, path)
+    out, lse = va.verify_attn_segmented(
+        w.q.cuda(), kv_dev, torch.from_numpy(ind).cuda(), torch.from_numpy(kip).cuda(),
+        torch.from_numpy(loc).cuda(), custom_mask=torch.from_numpy(mask).cuda(),
+        draft_kv=draft.cuda(), sm_scale=w.spec.sm_scale, nsplit=ns, flags=path, workspace=ws)
+    assert va.read_status(ws) == 0
+    want_pool = oracle.append_rows(synth.as_u16(pool0), synth.as_u16(draft), loc)
+    assert np.array_equal(synth.as_u16(kv_dev.cpu()), want_pool)
+    slots, indptr, prefix = oracle.segmented_lists(ind, kip, loc, spec.T)
+    bits, _ = oracle.dense_mask_bits(mask, kip, spec.T)
+    ref_o, ref_l, _ = oracle.verify_attn(synth.as_u16(w.q), want_pool, slots, indptr, prefix, bits,
+                                         w.spec.sm_scale)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("spec", [
+    synth.Spec("app_tp8", B=1, H=8, T=16, prefix=[4096], num_slots=1 << 15, seed=71),
+    synth.Spec("app_ragged", B=3, H=8, T=9, prefix=[0, 300, 77], num_slots=8192, seed=72),
+    synth.Spec("app_long", B=1, H=8, T=16, prefix=[20000], num_slots=1 << 16, seed=73),
+], ids=["tp8", "ragged", "long"])
+def test_segmented_append_then_verify(va, spec, path):
+    _append_case(va, spec, path)
+
+
+def test_segmented_append_wide_rows(va):
+    """Pool rows wider than 576: only the first 576 columns are written."""
+    _append_case(va, synth.Spec("app_wide", B=2, H=8, T=8, prefix=[500, 64], num_slots=4096,
+                                seed=74), 0, stride=640)
+
+
+def test_segmented_append_in_a_replayed_graph(va):
+    """One captured call, replayed with new draft rows each time: every replay
+    verifies against the rows it was given."""
+    spec = synth.Spec("app_graph", B=1, H=8, T=16, prefix=[2048], num_slots=1 << 14, seed=75)
+    w = synth.make(spec)
+    ind, kip, loc = _split(w)
+    mask = _flat_mask(w)
+    dev = "cuda"
+    q, kv = w.q.to(dev), w.kv_pool.to(dev)
+    ind_d, kip_d, loc_d = (torch.from_numpy(x).to(dev) for x in (ind, kip, loc))
+    mask_d = torch.from_numpy(mask).to(dev)
+    draft = torch.zeros(spec.T, synth.D_QK, dtype=torch.bfloat16, device=dev)
+    ws, ns = va.alloc_workspace(spec.B, spec.T, spec.H, 0)
+    out = torch.empty(spec.T, spec.H, synth.D_V, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(spec.T, spec.H, dtype=torch.float32, device=dev)
+
+    def call(stream=None):
+        va.verify_attn_segmented(q, kv, ind_d, kip_d, loc_d, custom_mask=mask_d, draft_kv=draft,
+                                 sm_scale=w.spec.sm_scale, nsplit=ns, workspace=ws, out=out,
+                                 lse=lse, stream=stream)
+
+    call()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(stream=s)
+    slots, indptr, prefix = oracle.segmented_lists(ind, kip, loc, spec.T)
+    bits, _ = oracle.dense_mask_bits(mask, kip, spec.T)
+    for k in range(3):
+        gen = torch.Generator().manual_seed(500 + k)
+        rows = torch.randn(spec.T, synth.D_QK, generator=gen).to(torch.bfloat16)
+        draft.copy_(rows)
+        g.replay()
+        torch.cuda.synchronize()
+        pool_k = oracle.append_rows(synth.as_u16(w.kv_pool), synth.as_u16(rows), loc)
+        ref_o, ref_l, _ = oracle.verify_attn(synth.as_u16(w.q), pool_k, slots, indptr, prefix,
+                                             bits, w.spec.sm_scale)
+        _gpu.compare(out, lse, ref_o, ref_l)

@@ -190,6 +190,16 @@ def test_dense_mask_bits_short_mask_reads_zero(oracle_mod):
     assert missing == 1 and bits.tolist() == [[3, 1]]
 
 
+def test_append_rows_small(oracle_mod):
+    pool = np.arange(4 * 6, dtype=np.uint16).reshape(4, 6)
+    rows = np.array([[100, 101, 102], [200, 201, 202], [300, 301, 302]], dtype=np.uint16)
+    out = oracle_mod.append_rows(pool, rows, [2, 9, 0])      # slot 9 is outside the pool
+    want = pool.copy()
+    want[2, :3] = [100, 101, 102]
+    want[0, :3] = [300, 301, 302]
+    assert np.array_equal(out, want) and np.array_equal(pool, np.arange(24).reshape(4, 6))
+
+
 def test_segmented_attention_is_slot_relocation_invariant(oracle_mod):
     """Draft rows moved to other pool slots, with out_cache_loc following them,
     give bit-identical attention."""
