@@ -667,6 +667,46 @@ def main():
         configs["segmented TP8 H=8 T=16 P=4096 (kv_indices + out_cache_loc + dense mask; "
                 "with the draft rows appended in the call) vs paged"] = seg
         torch.cuda.empty_cache()
+        # greedy tree acceptance after verify: B=8 requests, T=16 nodes, a
+        # 129280-token vocabulary, fp32 logits (one row after the prefix and
+        # one per node); rotated logits buffers larger than L2 together
+        ga = torch.Generator().manual_seed(9)
+        Ba, Ta, Va = 8, 16, 129280
+        nbuf = max(2, math.ceil(3 * torch.cuda.get_device_properties(dev).L2_cache_size
+                                / (Ba * (Ta + 1) * Va * 4)))
+        bufs = [(torch.randn(Ba, Va, generator=ga).to(dev), torch.randn(Ba, Ta, Va, generator=ga).to(dev))
+                for _ in range(nbuf)]
+        par_a = torch.stack([synth.make_parents(Ta, "random", ga) for _ in range(Ba)]).to(dev)
+        tok_a = torch.randint(0, Va, (Ba, Ta), generator=ga, dtype=torch.int32).to(dev)
+        slot_a = torch.arange(Ba * Ta, dtype=torch.int32, device=dev).reshape(Ba, Ta)
+        res = va.tree_accept(bufs[0][0], bufs[0][1], tok_a, par_a, slot_a)
+        ws_a, outs_a = res[4], res[:4]
+        # graphs of 8 calls, each on its own logits buffer, as for the verify step
+        sa = torch.cuda.Stream()
+        sa.wait_stream(torch.cuda.current_stream())
+        ga_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga_graph, stream=sa):
+            for k in range(8):
+                va.tree_accept(bufs[k % nbuf][0], bufs[k % nbuf][1], tok_a, par_a, slot_a,
+                               workspace=ws_a, outputs=outs_a, stream=sa)
+        for _ in range(3):
+            ga_graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        e0.record()
+        for _ in range(reps):
+            ga_graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        a_us = e0.elapsed_time(e1) / (8 * reps) * 1e3
+        a_bytes = Ba * (Ta + 1) * Va * 4
+        configs["tree acceptance B=8 T=16 V=129280 fp32 logits"] = {
+            "us": a_us, "logits_bytes": a_bytes, "gbs": a_bytes / (a_us * 1e-6) / 1e9,
+            "frac_hbm": a_bytes / (a_us * 1e-6) / 1e9 / hbm_peak,
+            "timing": "CUDA graphs of 8 calls on rotated logits buffers (> L2 together), events"}
+        del bufs
+        torch.cuda.empty_cache()
         # defrag: 65536 scattered rows (lower half of the pool) compacted into a
         # contiguous range in the upper half
         gd = torch.Generator().manual_seed(7)

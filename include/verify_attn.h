@@ -214,6 +214,43 @@ int verify_attn_segmented(const void *q, const void *kv_pool, int64_t num_slots,
                           size_t workspace_bytes, void *out, float *lse, va_stream_t stream);
 
 /*
+ * Greedy tree acceptance after verify (The Milestone Commit, "Input Knowledge
+ * Required": the verify step checks whether the draft predictions are
+ * correct; The Checkpoint Report, "Input Knowledge Required to Understand
+ * This Message": a drafter proposes a tree of candidate tokens, the target
+ * model checks them in one parallel pass).  For request b:
+ *   t = argmax(root_logits[b]); cur = the prefix; n = 0
+ *   repeat: among the draft nodes whose parent is cur (parent -1: the
+ *     prefix), take the lowest-numbered one whose draft token is t; if there
+ *     is none, stop; else accept it (accept_nodes[b*T + n++] = it), cur = it,
+ *     t = argmax(logits[b, it]).
+ *   accept_len[b] = n; bonus_token[b] = t (the target's token after the
+ *   accepted path); accept_nodes past n = -1.
+ * argmax = the lowest index among the largest non-NaN values (0 when a row is
+ * all NaN).  A node whose parent is not an earlier node counts as a child of
+ * the prefix and sets VA_STATUS_BAD_PARENT in the workspace status word.
+ *   root_logits   float [B, V] device: the target's logits at the last prefix
+ *                 position (the token after the prefix).
+ *   logits        float [B, T, V] device: its logits at each draft node.
+ *   draft_tokens  int32 [B, T] device: the token each draft node carries.
+ *   tree_parent   int32 [B, T] device, as for the verify calls.
+ *   draft_slots   int32 [B, T] device or NULL: each node's pool slot (e.g.
+ *                 out_cache_loc); accept_slots[b*T + m] = the slot of
+ *                 accept_nodes[b*T + m] (-1 past n, and everywhere when
+ *                 draft_slots is NULL).  accept_slots may be NULL.
+ *   workspace     device, >= va_tree_accept_workspace_bytes(B, T, V) bytes,
+ *                 256-byte aligned; first 4 bytes: the status word.
+ *   accept_len, bonus_token  int32 [B]; accept_nodes  int32 [B, T].
+ * 1 <= T <= 64, 1 <= V < 2^31 - 1.  Reads every logit once (HBM-bound).
+ */
+size_t va_tree_accept_workspace_bytes(int B, int T, int64_t V);
+int va_tree_accept(const float *root_logits, const float *logits, int64_t V,
+                   const int32_t *draft_tokens, const int32_t *tree_parent,
+                   const int32_t *draft_slots, int B, int T, void *workspace,
+                   size_t workspace_bytes, int32_t *accept_len, int32_t *accept_nodes,
+                   int32_t *accept_slots, int32_t *bonus_token, va_stream_t stream);
+
+/*
  * KV defragmentation (The Checkpoint Report, "Input Knowledge Required" and
  * "The Architecture of the Report": the deferred defragmentation phase).
  * For every request b and i < n_b = src_indptr[b+1] - src_indptr[b]:

@@ -79,6 +79,10 @@ def load() -> ctypes.CDLL:
     lib.verify_attn_segmented.argtypes = [P, P, i64, i64, P, P, P, P, P, i64, P, P, i32, i32,
                                           i32, f32, i32, i32, P, sz, P, P, P]
     lib.verify_attn_segmented.restype = i32
+    lib.va_tree_accept_workspace_bytes.argtypes = [i32, i32, i64]
+    lib.va_tree_accept_workspace_bytes.restype = sz
+    lib.va_tree_accept.argtypes = [P, P, i64, P, P, P, i32, i32, P, sz, P, P, P, P, P]
+    lib.va_tree_accept.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
     lib.verify_attn_paged_noalloc.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32,
@@ -302,6 +306,51 @@ def verify_attn_defrag(kv_pool: torch.Tensor, src_slots: torch.Tensor, src_indpt
         _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(src_slots), _ptr(src_indptr),
         _ptr(dst_base), _ptr(slot_idx_out), B, rows, _ptr(status), _stream(stream))
     _check("verify_attn_defrag", rc)
+
+
+def tree_accept(root_logits: torch.Tensor, logits: torch.Tensor, draft_tokens: torch.Tensor,
+                tree_parent: torch.Tensor, draft_slots: Optional[torch.Tensor] = None, *,
+                workspace: Optional[torch.Tensor] = None, outputs=None, stream=None):
+    """Greedy tree acceptance after verify.
+
+    root_logits fp32 [B, V] (the target's logits at the last prefix position),
+    logits fp32 [B, T, V] (at each draft node), draft_tokens int32 [B, T],
+    tree_parent int32 [B, T], draft_slots int32 [B, T] or None.  Returns
+    (accept_len int32 [B], accept_nodes int32 [B, T], accept_slots int32 [B, T],
+    bonus_token int32 [B], workspace); see va_tree_accept in verify_attn.h.
+    `outputs` = (accept_len, accept_nodes, accept_slots, bonus_token) tensors to
+    write into instead of new ones.
+    """
+    init(logits.device.index)
+    _dev(root_logits, "root_logits", torch.float32)
+    _dev(logits, "logits", torch.float32)
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    _dev(tree_parent, "tree_parent", torch.int32)
+    if draft_slots is not None:
+        _dev(draft_slots, "draft_slots", torch.int32)
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, T, V]")
+    B, T, V = logits.shape
+    if workspace is None:
+        n = load().va_tree_accept_workspace_bytes(B, T, V)
+        if n == 0:
+            raise VaError("va_tree_accept_workspace_bytes", -2)
+        workspace = torch.empty(n, dtype=torch.uint8, device=logits.device)
+    dev = logits.device
+    if outputs is None:
+        outputs = (torch.empty(B, dtype=torch.int32, device=dev),
+                   torch.empty(B, T, dtype=torch.int32, device=dev),
+                   torch.empty(B, T, dtype=torch.int32, device=dev),
+                   torch.empty(B, dtype=torch.int32, device=dev))
+    alen, nodes, slots, bonus = outputs
+    for t, name in zip(outputs, ("accept_len", "accept_nodes", "accept_slots", "bonus_token")):
+        _dev(t, name, torch.int32)
+    rc = load().va_tree_accept(_ptr(root_logits), _ptr(logits), V, _ptr(draft_tokens),
+                               _ptr(tree_parent), _ptr(draft_slots), B, T, _ptr(workspace),
+                               workspace.numel(), _ptr(alen), _ptr(nodes), _ptr(slots),
+                               _ptr(bonus), _stream(stream))
+    _check("va_tree_accept", rc)
+    return alen, nodes, slots, bonus, workspace
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

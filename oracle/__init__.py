@@ -22,6 +22,11 @@ Functions and the passages they follow (page titles and sections):
                    "The Deeper Significance" (reduction kernel).
   defrag        -- The Checkpoint Report, "Input Knowledge Required" (KV
                    defragmentation keeps per-request KV contiguous).
+  tree_accept   -- The Milestone Commit, "Input Knowledge Required" (the verify
+                   step checks whether the draft predictions are correct); The
+                   Checkpoint Report, "Input Knowledge Required to Understand
+                   This Message" (a drafter proposes a tree of candidate tokens,
+                   the target model checks them in one parallel pass).
   segmented_lists, dense_mask_bits, append_rows
                 -- The Checkpoint Report, "Mistakes and Incorrect Assumptions"
                    (the extend call takes the prefix slots in kv_indices, the
@@ -237,6 +242,57 @@ def append_rows(pool_bits, rows_bits, slots):
         if 0 <= s < pool.shape[0]:
             pool[s, :rows.shape[1]] = rows[r]
     return pool
+
+
+def target_token(row) -> int:
+    """The target's greedy token for one logits row: the lowest index among the
+    largest non-NaN values, 0 when every value is NaN."""
+    best, idx = None, 0
+    for i, v in enumerate(np.asarray(row, dtype=np.float64).tolist()):
+        if v != v:                 # NaN
+            continue
+        if best is None or v > best:
+            best, idx = v, i
+    return idx
+
+
+def tree_accept(root_logits, logits, tokens, parent, slots=None):
+    """Greedy acceptance of each request's draft tree.
+
+    Starting at the prefix with the target's token after it, repeatedly accept
+    the lowest-numbered child of the current position whose draft token is the
+    target's token there; stop when no child matches.  A node whose parent is
+    not an earlier node counts as a child of the prefix.  Returns
+    (accept_len [B], accept_nodes [B, T] (-1 padded), accept_slots [B, T]
+    (-1 padded; all -1 without slots), bonus [B], #bad parents).
+    """
+    rl = np.asarray(root_logits)
+    lg = np.asarray(logits)
+    tk = np.asarray(tokens).tolist()
+    par = np.asarray(parent).tolist()
+    sl = None if slots is None else np.asarray(slots).tolist()
+    B, T = lg.shape[0], lg.shape[1]
+    alen = np.zeros(B, dtype=np.int64)
+    nodes = -np.ones((B, T), dtype=np.int64)
+    aslots = -np.ones((B, T), dtype=np.int64)
+    bonus = np.zeros(B, dtype=np.int64)
+    bad = 0
+    for b in range(B):
+        p = [q if -1 <= q < i else -1 for i, q in enumerate(par[b])]
+        bad += sum(1 for i, q in enumerate(par[b]) if not (-1 <= q < i))
+        cur, n, t = -1, 0, target_token(rl[b])
+        while True:
+            kids = [c for c in range(T) if p[c] == cur and tk[b][c] == t]
+            if not kids:
+                break
+            c = kids[0]
+            nodes[b, n] = c
+            if sl is not None:
+                aslots[b, n] = sl[b][c]
+            n += 1
+            cur, t = c, target_token(lg[b, c])
+        alen[b], bonus[b] = n, t
+    return alen, nodes, aslots, bonus, bad
 
 
 def defrag(pool_bits, src_slots, src_indptr, dst_base):

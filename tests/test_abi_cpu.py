@@ -165,3 +165,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(va, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         va.load()
+
+
+def test_tree_accept_workspace_and_errors(lib):
+    lib.va_tree_accept_workspace_bytes.restype = ctypes.c_size_t
+    lib.va_tree_accept_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64]
+    n = lib.va_tree_accept_workspace_bytes(8, 16, 129280)
+    assert n > 256
+    assert lib.va_tree_accept_workspace_bytes(0, 16, 100) == 0
+    assert lib.va_tree_accept_workspace_bytes(1, 65, 100) == 0
+    assert lib.va_tree_accept_workspace_bytes(1, 16, 0) == 0
+    f = lib.va_tree_accept
+    P = ctypes.c_void_p
+    f.argtypes = [P, P, ctypes.c_int64, P, P, P, ctypes.c_int, ctypes.c_int, P, ctypes.c_size_t,
+                  P, P, P, P, P]
+    base = [A16, A16, 1000, A16, A16, None, 2, 8, A256, 1 << 20, A16, A16, None, A16, None]
+    for i in (0, 1, 3, 4, 8, 10, 11, 13):
+        bad = list(base); bad[i] = None
+        assert f(*bad) == -1
+    bad = list(base); bad[7] = 65
+    assert f(*bad) == -2
+    bad = list(base); bad[2] = 0
+    assert f(*bad) == -2
+    bad = list(base); bad[1] = A16 + 2
+    assert f(*bad) == -3
+    bad = list(base); bad[8] = A256 + 16
+    assert f(*bad) == -3
+    bad = list(base); bad[9] = 16
+    assert f(*bad) == -4

@@ -200,6 +200,83 @@ def test_append_rows_small(oracle_mod):
     assert np.array_equal(out, want) and np.array_equal(pool, np.arange(24).reshape(4, 6))
 
 
+def test_tree_accept_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "accept_small.txt"))
+    ints = lambda k: [int(x) for x in g[k].split()]
+    T = len(ints("parent"))
+    root = np.array([[float(x) for x in g["root"].split()]])
+    lg = np.array([[[float(x) for x in g[f"node{i}"].split()] for i in range(T)]])
+    alen, nodes, aslots, bonus, bad = oracle_mod.tree_accept(
+        root, lg, [ints("tokens")], [ints("parent")], [ints("slots")])
+    assert bad == 0
+    assert alen.tolist() == [int(g["accept_len"])]
+    assert nodes[0].tolist() == ints("accept_nodes")
+    assert aslots[0].tolist() == ints("accept_slots")
+    assert bonus.tolist() == [int(g["bonus"])]
+
+
+def _nan_argmax(row):
+    row = np.asarray(row, dtype=np.float64)
+    return 0 if np.isnan(row).all() else int(np.nanargmax(row))
+
+
+def test_target_token_is_nanargmax(oracle_mod):
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        row = rng.integers(0, 4, size=int(rng.integers(1, 40))).astype(np.float64)
+        row[rng.random(row.shape[0]) < 0.2] = np.nan
+        if rng.random() < 0.1:
+            row[:] = np.nan
+        assert oracle_mod.target_token(row) == _nan_argmax(row)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tree_accept_is_the_longest_matching_root_path(oracle_mod, seed):
+    """With distinct tokens among siblings, the accepted path is the longest
+    root path whose every token is the target's token at its parent (found
+    here by checking every node's path), and the bonus token is the target's
+    token at its end."""
+    rng = np.random.default_rng(seed)
+    B, T, V = 6, 12, 16          # V > T: a free token always exists among siblings
+    root = rng.normal(size=(B, V))
+    lg = rng.normal(size=(B, T, V))
+    parents = np.array([[rng.integers(-1, i) for i in range(T)] for _ in range(B)])
+    tokens = np.zeros((B, T), dtype=np.int64)
+    for b in range(B):
+        for c in range(T):
+            sib = [tokens[b, d] for d in range(c) if parents[b, d] == parents[b, c]]
+            want = _nan_argmax(root[b] if parents[b, c] < 0 else lg[b, parents[b, c]])
+            # often the target's token, never a sibling's
+            tok = want if (rng.random() < 0.7 and want not in sib) else int(rng.integers(0, V))
+            while tok in sib:
+                tok = (tok + 1) % V
+            tokens[b, c] = tok
+    alen, nodes, _, bonus, _ = oracle_mod.tree_accept(root, lg, tokens, parents)
+    for b in range(B):
+        best = []
+        for c in range(T):
+            path, k = [], c
+            while k >= 0:
+                path.append(k)
+                k = parents[b, k]
+            path = path[::-1]
+            ok = tokens[b, path[0]] == _nan_argmax(root[b]) and all(
+                tokens[b, path[m + 1]] == _nan_argmax(lg[b, path[m]]) for m in range(len(path) - 1))
+            if ok and len(path) > len(best):
+                best = path
+        assert alen[b] == len(best) and nodes[b, :len(best)].tolist() == best
+        end = _nan_argmax(lg[b, best[-1]]) if best else _nan_argmax(root[b])
+        assert bonus[b] == end
+
+
+def test_tree_accept_bad_parent_hangs_off_the_prefix(oracle_mod):
+    root = np.array([[0.0, 5.0]])
+    lg = np.zeros((1, 3, 2))
+    lg[0, 2, 0] = 1.0
+    alen, nodes, _, bonus, bad = oracle_mod.tree_accept(root, lg, [[0, 0, 1]], [[-1, 0, 2]])
+    assert bad == 1 and alen.tolist() == [1] and nodes[0, 0] == 2 and bonus.tolist() == [0]
+
+
 def test_segmented_attention_is_slot_relocation_invariant(oracle_mod):
     """Draft rows moved to other pool slots, with out_cache_loc following them,
     give bit-identical attention."""
