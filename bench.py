@@ -106,6 +106,21 @@ def run_case(va, args, dev):
           f"(eager launches, not the benchmark figure)", flush=True)
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x: the job takes as long as its slowest rank."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_rank_step: int, steps: int, ms: float) -> float:
+    """Whole-job GB/s of `world` replicas, each moving bytes_per_rank_step per step,
+    `steps` steps in `ms` (the slowest rank's time): weak scaling."""
+    return world * bytes_per_rank_step * steps / (ms / 1e3) / 1e9
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -521,12 +536,9 @@ def main():
     t_wall1 = time.time()
     time.sleep(0.25)
     clocks.stop()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
-    value = world * kv_step * args.steps / (ms / 1e3) / 1e9
+    value = job_gbs(world, kv_step, args.steps, ms)
 
     # ---- end to end through the public API with host buffers.  A step's
     # inputs (q, its slot table, indptr, prefix lengths, parents) are packed
@@ -596,8 +608,8 @@ def main():
             e2e_step(k)
         b.record()
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b) / Ke
-        e2e = {"value": world * kv_step / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e_ms = max_over_ranks(a.elapsed_time(b) / Ke, dist, dev)
+        e2e = {"value": job_gbs(world, kv_step, 1, e_ms), "unit": "GB/s",
                "us_per_step": e_ms * 1e3, "steps": Ke, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "note": "inputs packed in one pinned buffer (one H2D copy), out and lse read "
