@@ -545,75 +545,73 @@ def main():
     # in one pinned host buffer and land with one host-to-device copy in a
     # device buffer whose views the call takes; out and lse are views of one
     # device result buffer read back with one device-to-host copy.
-    e2e = None
-    if True:
-        def align(n):
-            return (n + 255) // 256 * 256
+    def align(n):
+        return (n + 255) // 256 * 256
 
-        parts = [("q", step.q), ("tab", step.tables[0]), ("par", step.parents),
-                 ("ind", step.indptr), ("pre", step.prefix)]
-        offs, o = {}, 0
+    parts = [("q", step.q), ("tab", step.tables[0]), ("par", step.parents),
+             ("ind", step.indptr), ("pre", step.prefix)]
+    offs, o = {}, 0
+    for name, t in parts:
+        offs[name] = (o, t.numel() * t.element_size())
+        o = align(o + t.numel() * t.element_size())
+    in_bytes = o
+
+    def pack(tab):
+        hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
         for name, t in parts:
-            offs[name] = (o, t.numel() * t.element_size())
-            o = align(o + t.numel() * t.element_size())
-        in_bytes = o
-
-        def pack(tab):
-            hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-            for name, t in parts:
-                src = tab if name == "tab" else t
-                off, n = offs[name]
-                hb[off:off + n] = src.detach().cpu().contiguous().view(-1).view(torch.uint8)
-            return hb
-
-        hins = [pack(t) for t in step.tables]
-        dbuf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-
-        def dview(name, like):
+            src = tab if name == "tab" else t
             off, n = offs[name]
-            return dbuf[off:off + n].view(like.dtype).view(like.shape)
+            hb[off:off + n] = src.detach().cpu().contiguous().view(-1).view(torch.uint8)
+        return hb
 
-        dq, dtab = dview("q", step.q), dview("tab", step.tables[0])
-        dpar, dind, dpre = dview("par", step.parents), dview("ind", step.indptr), dview("pre", step.prefix)
-        o_bytes = step.out.numel() * step.out.element_size()
-        l_off = align(o_bytes)
-        res_bytes = l_off + step.lse.numel() * step.lse.element_size()
-        dres = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
-        dout = dres[:o_bytes].view(step.out.dtype).view(step.out.shape)
-        dlse = dres[l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
-        hres = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
-        h2d = in_bytes
-        d2h = res_bytes
-        Ke = min(args.steps, 500)
+    hins = [pack(t) for t in step.tables]
+    dbuf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
 
-        def e2e_step(k):
-            dbuf.copy_(hins[k % len(hins)], non_blocking=True)
-            va.verify_attn_paged(dq, step.pool, dtab, dind, dpre, dpar, sm_scale=synth.SM_SCALE,
-                                 nsplit=step.nsplit, flags=step.path, workspace=step.ws,
-                                 out=dout, lse=dlse)
-            hres.copy_(dres, non_blocking=True)
+    def dview(name, like):
+        off, n = offs[name]
+        return dbuf[off:off + n].view(like.dtype).view(like.shape)
 
-        for k in range(min(args.warmup, 20)):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        # the packed copy path computes the same step: check one result
-        e2e_step(0)
-        torch.cuda.synchronize()
-        step.call(0)
-        torch.cuda.synchronize()
-        assert torch.equal(dout, step.out) and torch.equal(dlse, step.lse), "e2e path differs"
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for k in range(Ke):
-            e2e_step(k)
-        b.record()
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(a.elapsed_time(b) / Ke, dist, dev)
-        e2e = {"value": job_gbs(world, kv_step, 1, e_ms), "unit": "GB/s",
-               "us_per_step": e_ms * 1e3, "steps": Ke, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h),
-               "note": "inputs packed in one pinned buffer (one H2D copy), out and lse read "
-                       "back with one D2H copy, every step"}
+    dq, dtab = dview("q", step.q), dview("tab", step.tables[0])
+    dpar, dind, dpre = dview("par", step.parents), dview("ind", step.indptr), dview("pre", step.prefix)
+    o_bytes = step.out.numel() * step.out.element_size()
+    l_off = align(o_bytes)
+    res_bytes = l_off + step.lse.numel() * step.lse.element_size()
+    dres = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
+    dout = dres[:o_bytes].view(step.out.dtype).view(step.out.shape)
+    dlse = dres[l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
+    hres = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
+    h2d = in_bytes
+    d2h = res_bytes
+    Ke = min(args.steps, 500)
+
+    def e2e_step(k):
+        dbuf.copy_(hins[k % len(hins)], non_blocking=True)
+        va.verify_attn_paged(dq, step.pool, dtab, dind, dpre, dpar, sm_scale=synth.SM_SCALE,
+                             nsplit=step.nsplit, flags=step.path, workspace=step.ws,
+                             out=dout, lse=dlse)
+        hres.copy_(dres, non_blocking=True)
+
+    for k in range(min(args.warmup, 20)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    # the packed copy path computes the same step: check one result
+    e2e_step(0)
+    torch.cuda.synchronize()
+    step.call(0)
+    torch.cuda.synchronize()
+    assert torch.equal(dout, step.out) and torch.equal(dlse, step.lse), "e2e path differs"
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for k in range(Ke):
+        e2e_step(k)
+    b.record()
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(a.elapsed_time(b) / Ke, dist, dev)
+    e2e = {"value": job_gbs(world, kv_step, 1, e_ms), "unit": "GB/s",
+           "us_per_step": e_ms * 1e3, "steps": Ke, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h),
+           "note": "inputs packed in one pinned buffer (one H2D copy), out and lse read "
+                   "back with one D2H copy, every step"}
 
     # ---- prefix sweeps (H=8 and H=64, T=16), scattered slots
     sweep = []
