@@ -67,6 +67,12 @@ SWEEP = [
     (2, 16, 4, [513, 1], "random", 0),
     (1, 64, 2, [2049], "random", 0),
     (1, 5, 13, [777], "random", 0),
+    # several 128-row blocks with a ragged last one
+    (1, 24, 10, [3000], "random", 0),
+    (2, 40, 7, [100, 2500], "random", 3),
+    (1, 128, 2, [700], "flat", 0),
+    # many short requests: the split rule's several-waves regime
+    (16, 8, 4, [0, 5, 64, 65, 127, 128, 129, 300, 1, 2, 3, 511, 512, 513, 40, 90], "random", 0),
 ]
 
 
