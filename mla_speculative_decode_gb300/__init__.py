@@ -169,20 +169,39 @@ def _tree_args(tree_parent, tree_bits):
     return _ptr(tree_parent), _ptr(tree_bits)
 
 
-def verify_attn_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor,
-                      kv_indptr: torch.Tensor, prefix_len: torch.Tensor,
-                      tree_parent: Optional[torch.Tensor] = None,
-                      tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
-                      nsplit: int = 0, flags: int = PATH_AUTO,
-                      workspace: Optional[torch.Tensor] = None,
-                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Paged MLA tree-verify attention; returns (out bf16 [B*T, H, 512], lse fp32 [B*T, H]).
+class PreparedCall:
+    """One verify call whose arguments were checked and marshalled once.
 
-    q [B*T, H, 576] bf16; kv_pool [num_slots, stride] bf16; slot_idx int32;
-    kv_indptr int32 [B+1]; prefix_len int32 [B]; tree_parent int32 [B, T] or
-    tree_bits int64 [B, T] (bit patterns of uint64 masks).  All CUDA tensors.
+    Calling it launches the step again on the same buffers, whose contents may
+    change between calls (new queries, slot tables, trees copied into them), on
+    the stream it was prepared for: the host work per step is one C call.  The
+    tensors it refers to must stay alive; `out` and `lse` are its outputs.
     """
+
+    def __init__(self, name: str, args: tuple, out: torch.Tensor, lse: torch.Tensor, keep: tuple):
+        self._fn = getattr(load(), name)
+        self._name = name
+        self._args = args
+        self.out, self.lse = out, lse
+        self._keep = keep          # the tensors behind the pointers
+
+    def __call__(self) -> Tuple[torch.Tensor, torch.Tensor]:
+        rc = self._fn(*self._args)
+        if rc < 0:
+            raise VaError(self._name, rc)
+        return self.out, self.lse
+
+
+def prepare_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor,
+                  kv_indptr: torch.Tensor, prefix_len: torch.Tensor,
+                  tree_parent: Optional[torch.Tensor] = None,
+                  tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                  nsplit: int = 0, flags: int = PATH_AUTO,
+                  workspace: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  stream=None) -> PreparedCall:
+    """verify_attn_paged's checks and marshalling, done once: returns a
+    PreparedCall that launches the step on these buffers each time it is called."""
     init(q.device.index)
     _dev(q, "q", torch.bfloat16)
     _dev(kv_pool, "kv_pool", torch.bfloat16)
@@ -198,12 +217,31 @@ def verify_attn_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Te
         workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
     out, lse = _outputs(q.shape[0], H, q.device, out, lse)
     par, bits = _tree_args(tree_parent, tree_bits)
-    rc = load().verify_attn_paged(
-        _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
-        _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,
-        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
-    _check("verify_attn_paged", rc)
-    return out, lse
+    args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
+            _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,
+            _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
+    return PreparedCall("verify_attn_paged", args, out, lse,
+                        (q, kv_pool, slot_idx, kv_indptr, prefix_len, tree_parent, tree_bits,
+                         workspace))
+
+
+def verify_attn_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor,
+                      kv_indptr: torch.Tensor, prefix_len: torch.Tensor,
+                      tree_parent: Optional[torch.Tensor] = None,
+                      tree_bits: Optional[torch.Tensor] = None, *, sm_scale: float,
+                      nsplit: int = 0, flags: int = PATH_AUTO,
+                      workspace: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA tree-verify attention; returns (out bf16 [B*T, H, 512], lse fp32 [B*T, H]).
+
+    q [B*T, H, 576] bf16; kv_pool [num_slots, stride] bf16; slot_idx int32;
+    kv_indptr int32 [B+1]; prefix_len int32 [B]; tree_parent int32 [B, T] or
+    tree_bits int64 [B, T] (bit patterns of uint64 masks).  All CUDA tensors.
+    """
+    return prepare_paged(q, kv_pool, slot_idx, kv_indptr, prefix_len, tree_parent, tree_bits,
+                         sm_scale=sm_scale, nsplit=nsplit, flags=flags, workspace=workspace,
+                         out=out, lse=lse, stream=stream)()
 
 
 def verify_attn_contiguous(q: torch.Tensor, kv_pool: torch.Tensor, kv_start: torch.Tensor,

@@ -457,3 +457,28 @@ def test_status_is_per_call_back_to_back(va, path):
     ref_o, ref_l = _gpu.reference(w)
     call(d_ok)
     _gpu.compare(out, lse, ref_o, ref_l)
+
+
+def test_prepared_call_relaunches_on_new_contents(va):
+    """A call prepared once and launched again after new queries, slots and
+    parents were copied into the same buffers computes the new step."""
+    s1 = synth.Spec("prep1", B=2, H=8, T=8, prefix=[300, 120], num_slots=4096, seed=81)
+    s2 = synth.Spec("prep2", B=2, H=8, T=8, prefix=[300, 120], num_slots=4096, seed=82)
+    w1, w2 = synth.make(s1), synth.make(s2)
+    d = _gpu.to_device(w1)
+    kv2 = w2.kv_pool.cuda()
+    call = va.prepare_paged(d["q"], kv2, d["slot_idx"], d["kv_indptr"], d["prefix_len"],
+                            d["parents"], sm_scale=s1.sm_scale)
+    out, lse = call()
+    torch.cuda.synchronize()
+    w1.kv_pool = w2.kv_pool          # both steps read the second pool
+    ref_o, ref_l = _gpu.reference(w1)
+    _gpu.compare(out, lse, ref_o, ref_l)
+    d["q"].copy_(w2.q)
+    d["slot_idx"].copy_(w2.slot_idx)
+    d["parents"].copy_(w2.parents)
+    out2, lse2 = call()
+    torch.cuda.synchronize()
+    assert out2.data_ptr() == out.data_ptr()
+    ref_o, ref_l = _gpu.reference(w2)
+    _gpu.compare(out2, lse2, ref_o, ref_l)
