@@ -29,8 +29,9 @@
  *  - Host-checkable argument errors return a negative VA_ERR_* code before any
  *    device work is enqueued.  Device-data errors (a slot outside the pool, a
  *    parent that is not an earlier node, a slot list shorter than
- *    prefix_len + T) set bits in the workspace status word; the offending key
- *    is skipped and the call still returns VA_OK.  Kernels never trap.
+ *    prefix_len + T, a dense mask shorter than its rows) set bits in the
+ *    workspace status word; the offending key or entry is skipped and the
+ *    call still returns VA_OK.  Kernels never trap.
  *  - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
  *  - Calls on distinct workspaces are thread-safe.
  */
