@@ -789,7 +789,7 @@ def main():
                      "frac": achieved / hbm_peak, "traffic": recorded_traffic(),
                      "kernel": "split-K partial", "kernel_us": k_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (3 if args.path == 1 else 2) * args.steps, "clocks": clk,
         "parity": parity, "sweep": sweep, "configs": configs,
     }
     if rank == 0:

@@ -105,6 +105,9 @@ int va_auto_nsplit(int B, int T, int H, int flags);
  * arithmetic, no CUDA call.  Layout (each region 256-byte aligned):
  *   [0, 256)        status word (uint32) and reserved header
  *   tree masks      uint64 [B*T]
+ *   CTA status      uint32 [B][ceil(T*H/128)][nsplit][2] (tensor-core path:
+ *                   each split-K CTA's status bits, OR-ed into the status
+ *                   word by the merge)
  *   partial lse     float  [nsplit][B*T*H]
  *   partial out     bf16   [nsplit][B*T*H][512] (normalised by the split's
  *                   row sum; merged in fp32)

@@ -136,6 +136,27 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
     *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + chunk * kCombineCols + lane * 4) = packed;
     if (chunk == 0 && lane == 0) p.lse[row] = L;
   }
+  if (p.cta_flags && row == 0 && chunk == 0) {
+    // tensor-core path: the call's status word is the OR of the status words
+    // of every split-K CTA that ran (splits past a request's effective count
+    // exit at once and write none)
+    __shared__ uint32_t acc;
+    if (tid == 0) acc = 0u;
+    __syncthreads();
+    const int rbs = (p.rows_per_req + 127) / 128;
+    uint32_t v = 0u;
+    for (int b = 0; b < p.B; ++b) {
+      const int ne = split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff;
+      const size_t base = size_t(b) * rbs * p.nsplit;
+      for (int i = tid; i < rbs * ne * 2; i += kCombineThreads) {
+        const int rb = i / (ne * 2), s = (i / 2) % ne, rank = i & 1;
+        v |= p.cta_flags[((base + size_t(rb) * p.nsplit) + s) * 2 + rank];
+      }
+    }
+    if (v) atomicOr(&acc, v);
+    __syncthreads();
+    if (tid == 0) *p.status = acc;
+  }
 }
 
 constexpr int kDefragThreads = 256;

@@ -29,6 +29,7 @@ __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / 
 // Workspace regions (byte offsets from the workspace base).
 struct WsLayout {
   size_t bits;   // uint64 [B*T]
+  size_t flags;  // uint32 [B][row blocks of 128][nsplit][2]: status bits of each split-K CTA
   size_t plse;   // float  [nsplit][rows]
   size_t po;     // bf16   [nsplit][rows][512]
   size_t total;
@@ -38,7 +39,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int H, int nsplit) {
   WsLayout L;
   const size_t rows = size_t(B) * T * H;
   L.bits = kHeaderBytes;
-  L.plse = L.bits + align256(size_t(B) * T * sizeof(uint64_t));
+  L.flags = L.bits + align256(size_t(B) * T * sizeof(uint64_t));
+  const size_t rbs = (size_t(T) * H + 127) / 128;
+  L.plse = L.flags + align256(size_t(B) * rbs * nsplit * 2 * sizeof(uint32_t));
   L.po = L.plse + align256(size_t(nsplit) * rows * sizeof(float));
   L.total = L.po + align256(size_t(nsplit) * rows * kDv * sizeof(__nv_bfloat16));
   return L;
@@ -68,6 +71,11 @@ struct Params {
   float* part_lse;             // [nsplit][rows]
   __nv_bfloat16* part_o;       // [nsplit][rows][512], normalised by the split's row sum
   uint32_t* status;
+  // Tensor-core path: each split-K CTA stores its status bits to its own word
+  // here ([B][row blocks][nsplit][2]) and the merge kernel writes their OR to
+  // *status, so no kernel has to clear *status first.  NULL on the FMA path,
+  // where the mask kernel clears *status and the kernels OR into it.
+  uint32_t* cta_flags;
   __nv_bfloat16* out;          // [rows, 512]
   float* lse;                  // [rows]
 };
@@ -102,7 +110,7 @@ struct ReqInfo {
   int64_t dbase; // segmented: draft key j >= P is draft_slots[dbase + j]
 };
 
-__device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
+__device__ inline ReqInfo req_info(const Params& p, int b, bool flag, bool* bad_out = nullptr) {
   ReqInfo r;
   r.dbase = 0;
   bool bad = false;
@@ -118,6 +126,7 @@ __device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
     r.base = i0;
     r.dbase = int64_t(b) * p.T - P;
     if (bad && flag) atomicOr(p.status, VA_STATUS_BAD_INDPTR);
+    if (bad_out) *bad_out = bad;
     return r;
   }
   int P = p.prefix_len[b];
@@ -139,6 +148,7 @@ __device__ inline ReqInfo req_info(const Params& p, int b, bool flag) {
   r.P = P;
   r.N = P + p.T;
   if (bad && flag) atomicOr(p.status, VA_STATUS_BAD_INDPTR);
+  if (bad_out) *bad_out = bad;
   return r;
 }
 

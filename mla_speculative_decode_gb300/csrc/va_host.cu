@@ -146,8 +146,15 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
 
-  if (va::launch_tree_bits(p, reinterpret_cast<uint64_t*>(w + L.bits), st) != cudaSuccess)
-    return VA_ERR_LAUNCH;
+  // The tensor-core path computes the masks in its split-K kernel and keeps
+  // per-CTA status words that the merge combines, so the mask kernel runs
+  // there only to append draft rows.  The FMA path reads the masks the mask
+  // kernel writes, and the mask kernel clears the status word for it.
+  if (path == VA_PATH_TC) p.cta_flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  if (path != VA_PATH_TC || p.draft_kv) {
+    if (va::launch_tree_bits(p, reinterpret_cast<uint64_t*>(w + L.bits), st) != cudaSuccess)
+      return VA_ERR_LAUNCH;
+  }
   const bool timed = g_ev_before && g_ev_after;
   if (timed && record_event(g_ev_before, st) != cudaSuccess) return VA_ERR_CUDA;
   cudaError_t e = path == VA_PATH_TC ? va::launch_partial_tc(p, ds.num_sms, st)

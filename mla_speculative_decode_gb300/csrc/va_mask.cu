@@ -5,9 +5,11 @@
 // the draft rows of the extend mask; "Input Knowledge Required": DDTree
 // verifies a tree of draft tokens in one pass).  For segmented calls it reads
 // the same sets out of the dense extend mask instead (the last T columns of
-// each draft row, stride prefix + q_len).  It also opens every verify call by
-// clearing the workspace status word, so it runs even when the caller
-// supplies the masks itself.
+// each draft row, stride prefix + q_len).  On the FMA path it also opens
+// every verify call by clearing the workspace status word, so it runs even
+// when the caller supplies the masks itself.  On the tensor-core path the
+// split-K kernel computes the masks itself and this kernel runs only to
+// append draft rows (its extra CTAs).
 //
 // One CTA; a warp per request.  The request's parents are staged in shared
 // memory and each lane builds its own node's set by walking up the tree
@@ -48,6 +50,9 @@ __global__ void __launch_bounds__(kWarps * 32) tree_bits_kernel(Params p, uint64
     }
     return;
   }
+  // tensor-core path: the split-K kernel computes the masks and the merge
+  // kernel writes the status word; this kernel only appends draft rows there
+  if (p.cta_flags) return;
   if (threadIdx.x == 0) *p.status = 0u;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -110,9 +110,12 @@ constexpr uint32_t kOffBars = 0;
 constexpr uint32_t kOffTmemSlot = 512;
 constexpr uint32_t kOffAbort = 516;
 constexpr uint32_t kOffCmd = 520;                           // PV: row-warp command word
+constexpr uint32_t kOffFlags = 524;                         // uint32: this CTA's status bits
+constexpr uint32_t kOffPar = 1024;                          // QK: int32 [64] tree parents
 constexpr uint32_t kOffValid = 576;                         // QK: uint64 [8] key-validity ring
 constexpr uint32_t kOffFin = 1024;                          // PV: float [128] 1 / row sum
 constexpr uint32_t kOffSrow = 1536;                         // int32 [2][64] staged pool rows
+static_assert(kOffPar + 4 * kTmax <= kOffSrow, "parents in the QK CTA's header");
 constexpr uint32_t kOffMx = 2048;                           // QK: float [2][128] half maxima
 constexpr uint32_t kOffK = 4096;                            // QK: K ring
 constexpr uint32_t kOffStage = kOffK + kRingK * kBlockBytes;   // QK: P staging [2]
@@ -199,14 +202,16 @@ __device__ __forceinline__ int checked_row(const Params& p, int raw) {
 // Completion: every producer's cp.async arrival (noinc) on the tile's full
 // barrier plus one arrival of producer 0 (carrying the TMA byte count when
 // boxes are used).  Returns false when a bounded wait gave up (all producers
-// agree through the named barrier).
+// agree through the named barrier).  Keys without a valid pool row set
+// VA_STATUS_BAD_SLOT in the CTA's status word `cta_flags` (shared memory).
 template <int kBlocks, int kRing, bool kMask>
 __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, const SplitRange& sr,
                                         int ntiles, int ptid, uint32_t ring, uint32_t full0,
                                         uint32_t empty0, int* srow, uint32_t* valid32,
                                         uint32_t vready0, volatile int* abort_flag,
                                         const CUtensorMap* map3, const CUtensorMap* map2,
-                                        bool box3d, uint32_t qready, int raw) {
+                                        bool box3d, uint32_t qready, int raw,
+                                        uint32_t* cta_flags) {
   constexpr int kChunks = kBlocks * 8;
   const int lane = ptid & 31;
   bool ok = true;
@@ -305,10 +310,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   }
   if (ptid == 0) VA_PH_STORE(kMask ? 11 : 12);
   cp_async_wait_all();
-  if (kMask && bad_slot) {
-    griddep_wait();
-    atomicOr(p.status, VA_STATUS_BAD_SLOT);
-  }
+  if (kMask && bad_slot) atomicOr(cta_flags, VA_STATUS_BAD_SLOT);
   return ok;
 }
 
@@ -369,9 +371,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   griddep_launch_dependents();   // the merge kernel may be scheduled as clusters retire
-  // The tree-mask kernel before this one clears the status word and writes
-  // the ancestor masks: every status write and every mask read below follows
-  // a griddep_wait(); the set-up, the Q load and the first gathers overlap it.
+  // The kernel computes its rows' ancestor masks itself and keeps its status
+  // bits in shared memory, stored to its own workspace word at the end; the
+  // merge kernel ORs those into the status word.  It is the call's first
+  // kernel, except when the call appends draft rows first: then the kernel
+  // before it writes them, and the producers wait (griddepcontrol.wait)
+  // before a tile holding draft keys.
   const ReqInfo ri = req_info(p, b, false);
   const SplitRange sr = split_range(ri.N, p.nsplit, split);
   if (split >= sr.nsplit_eff) return;   // both CTAs of the cluster leave together
@@ -385,10 +390,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // raw pool rows of the first tile (producers), loaded during the set-up
   const int raw0 = producer && ptid < 64 ? fetch_row(p, ri, sr.k0 + ptid, sr.k1) : -1;
 
+  uint32_t* cta_flags = reinterpret_cast<uint32_t*>(gb + kOffFlags);
   auto fail = [&]() {
     *abort_flag = 1;
-    griddep_wait();
-    atomicOr(p.status, VA_STATUS_TIMEOUT);
+    atomicOr(cta_flags, VA_STATUS_TIMEOUT);
   };
 
   if (tid == 0) {
@@ -400,6 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
+    *cta_flags = 0u;
     fence_mbar_init();
   }
   if (warp == 2) tmem_alloc(sb + kOffTmemSlot, kTmemCols);
@@ -420,7 +426,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            bar(B_EMPTY), srow,
                                            reinterpret_cast<uint32_t*>(gb + kOffValid),
                                            bar(B_VREADY), abort_flag, &tmap_k, &tmap_2d,
-                                           box3d != 0, bar(B_QREADY), raw0) &&
+                                           box3d != 0, bar(B_QREADY), raw0, cta_flags) &&
           ptid == 0)
         fail();
     } else if (warp == 1) {
@@ -484,18 +490,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
       // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of
       // every tile for row r
+      // the request's tree parents, staged for the ancestor walk below while
+      // Q is on its way
+      int* par = reinterpret_cast<int*>(gb + kOffPar);
+      if (p.tree_parent && tid - 128 < p.T) par[tid - 128] = p.tree_parent[size_t(b) * p.T + (tid - 128)];
       if (!load_q(half, q4, lane, tmem, sb + kOffQ, bar(B_QTMA), abort_flag) && tid == 128) fail();
       tc_fence_before();
       mbar_arrive(bar(B_QREADY));
-      griddep_wait();   // ancestor masks written, status cleared
-      if (split == 0 && rb == 0 && tid == 128) (void)req_info(p, b, true);
+      if (split == 0 && rb == 0 && tid == 128) {
+        bool bad = false;
+        (void)req_info(p, b, false, &bad);
+        if (bad) atomicOr(cta_flags, VA_STATUS_BAD_INDPTR);
+      }
       if (tid == 128) VA_TRACE_CTA(6, 5);
       const int r = q4 * 32 + lane;
       const int lr = row0 + r;
       const bool row_ok = lr < R;
       const bool issuer = warp == 4 && lane == 0;
       const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);
-      const uint64_t nbits = row_ok ? p.bits[size_t(b) * p.T + lr / p.H] : 0ull;
+      // The row's draft node and its ancestor-or-self set (bit k: draft node
+      // k), from the parents (a walk up the staged list: a node whose parent
+      // is not an earlier node hangs off the prefix and is flagged, and a walk
+      // stops below such a node), from the dense mask rows (the last T
+      // entries of the node's row; entries past the mask read as 0 and are
+      // flagged), or as the caller gave them.
+      named_sync(kSoftmaxBar, kSoftmax);   // parents staged
+      uint64_t nbits = 0ull;
+      if (row_ok) {
+        const int node = lr / p.H;
+        if (p.tree_parent) {
+          nbits = 1ull << node;
+          int q = par[node];
+          if (q < -1 || q >= node) {
+            atomicOr(cta_flags, VA_STATUS_BAD_PARENT);
+          } else {
+            while (q >= 0) {
+              nbits |= 1ull << q;
+              const int up = par[q];
+              if (up < -1 || up >= q) break;
+              q = up;
+            }
+          }
+        } else if (p.dense_mask) {
+          const int64_t first = p.kv_indptr[0];
+          const int64_t e0 = int64_t(p.T) * ((ri.base - first) + int64_t(b) * p.T) +
+                             int64_t(node) * (ri.P + p.T) + ri.P;
+          bool bad = false;
+          for (int k = 0; k < p.T; ++k) {
+            const int64_t e = e0 + k;
+            if (e >= 0 && e < p.dense_mask_len) {
+              if (p.dense_mask[e]) nbits |= 1ull << k;
+            } else {
+              bad = true;
+            }
+          }
+          if (bad) atomicOr(cta_flags, VA_STATUS_BAD_MASK);
+        } else {
+          nbits = p.bits[size_t(b) * p.T + node];
+        }
+      }
       float* mx = reinterpret_cast<float*>(gb + kOffMx);
       const uint32_t pv_p = mapa(sb + kOffP, 1);
       const uint32_t pv_pfull = mapa(bar(B_PFULL), 1);
@@ -633,7 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- producers: value columns of the same tiles
       if (!produce<kVBlocks, kRingV, false>(p, ri, sr, ntiles, ptid, sb + kOffV, bar(B_FULL),
                                             bar(B_EMPTY), srow, nullptr, 0u, abort_flag, &tmap_v,
-                                            &tmap_2d, box3d != 0, 0u, raw0) &&
+                                            &tmap_2d, box3d != 0, 0u, raw0, cta_flags) &&
           ptid == 0)
         fail();
       cluster_arrive_relaxed();   // done with the QK CTA (see the end of the kernel)
@@ -816,6 +869,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 2);
   tc_fence_before();
   __syncthreads();
+  // this CTA's status bits, for the merge kernel to OR into the status word
+  if (tid == 0)
+    p.cta_flags[((size_t(b) * gridDim.y + rb) * p.nsplit + split) * 2 + rank] = *cta_flags;
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 3);
   if (warp == 2) {
     tc_fence_after();
@@ -934,8 +990,9 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
     if (!encode_pool_map(&t2, p, 0)) return cudaErrorNotSupported;
     if (encode_pool_map(&tk, p, kKBlocks) && encode_pool_map(&tv, p, kVBlocks)) box3d = 1;
   }
-  // launched with programmatic stream serialization: the clusters start
-  // while the tree-mask kernel runs (see griddep_wait in the kernel)
+  // After the draft-row append kernel the clusters may start while it runs
+  // (programmatic stream serialization; see the producers' griddepcontrol.wait);
+  // as the call's first kernel, a plain launch after the stream's earlier work.
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(unsigned(2 * p.nsplit), unsigned(ceil_div(p.rows_per_req, kRows)), unsigned(p.B));
@@ -946,7 +1003,7 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.draft_kv ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p, tk, tv, t2, tq, box3d);
 }
 
