@@ -148,7 +148,8 @@ size_t va_workspace_bytes(int B, int T, int H, int nsplit);
  *   out           bf16 [B*T, H, 512], 16-byte aligned (round-to-nearest-even).
  *   lse           float [B*T, H]; -inf for a row that sees no key.
  *   stream        stream the kernels are launched on.
- * The status word is cleared by the call itself before any check runs.
+ * The status word describes this call only: every call rewrites it (no
+ * clearing by the caller), and it is complete once the call's work is.
  */
 int verify_attn_paged(const void *q, const void *kv_pool, int64_t num_slots,
                       int64_t kv_row_stride, const int32_t *slot_idx, const int32_t *kv_indptr,
