@@ -88,7 +88,9 @@ int va_version(void);
 /*
  * Caches the device's SM count and checks that it is an sm_103 part.  Call
  * once per device, outside stream capture, before the first verify call on
- * that device.  Returns VA_OK, VA_ERR_UNSUPPORTED or VA_ERR_CUDA.
+ * that device.  It also places the scratch array of
+ * verify_attn_paged_noalloc on the device (VA_NOALLOC_SCRATCH_BYTES; see
+ * there).  Returns VA_OK, VA_ERR_UNSUPPORTED or VA_ERR_CUDA.
  */
 int va_init(int device);
 
@@ -288,13 +290,18 @@ int verify_attn_defrag(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
  * Arguments are those of verify_attn_paged without workspace and
  * workspace_bytes; the caller still provides every input and out / lse.  The
  * scratch is a fixed device array of VA_NOALLOC_SCRATCH_BYTES inside the
- * library, one per GPU that loads it, held until the process exits.
+ * library.  va_init(device) places it on that device (the driver loads the
+ * library's device code lazily, so the array's memory is taken then) and
+ * resolves its device address with cudaGetSymbolAddress; from then on each
+ * GPU that was initialised holds the array until the process exits.  Call
+ * va_init before reserving the rest of device memory.
  *  - Sizes: with nsplit = 0 the split count is lowered until the scratch
  *    layout fits; an explicit nsplit whose layout does not fit, or sizes for
  *    which even one split does not fit, return VA_ERR_WORKSPACE.
- *  - First call on a device (after va_init on it) resolves the array's device
- *    address with cudaGetSymbolAddress; make that first call before any stream
- *    capture.  The first call is not thread-safe.
+ *  - If va_init could not place the array (no device memory left for it),
+ *    the first call on that device tries again and returns VA_ERR_CUDA if it
+ *    still cannot; such a first call must come before any stream capture and
+ *    is not thread-safe.
  *  - Every call shares the one array and leaves its contents behind; the call
  *    clears its status word itself.  Calls that overlap on the GPU (other
  *    streams, other threads) race on the array and must be serialised by the

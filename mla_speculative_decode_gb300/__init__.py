@@ -151,21 +151,44 @@ def alloc_workspace(B: int, T: int, H: int, nsplit: int = 0, flags: int = PATH_A
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda"), ns
 
 
+def _dims(q: torch.Tensor, B: int) -> Tuple[int, int]:
+    """(T, H) of a query tensor [B*T, H, 576] for B requests.  The C ABI takes
+    no tensor sizes, so a query block that does not split into B requests is
+    rejected here, before any pointer reaches the library."""
+    if q.dim() != 3 or q.shape[2] != D_QK:
+        raise ValueError(f"q must be [B*T, H, {D_QK}], got {tuple(q.shape)}")
+    if B < 1 or q.shape[0] % B != 0 or q.shape[0] == 0:
+        raise ValueError(f"q has {q.shape[0]} rows, not a positive multiple of B={B}")
+    return q.shape[0] // B, q.shape[1]
+
+
 def _outputs(rows: int, H: int, device, out, lse):
+    """Allocates out / lse when not given; a given one must have the step's
+    exact shape (the kernels write [rows, H, 512] and [rows, H] through a bare
+    pointer, so an undersized buffer would be written past its end)."""
     if out is None:
         out = torch.empty(rows, H, D_V, dtype=torch.bfloat16, device=device)
     if lse is None:
         lse = torch.empty(rows, H, dtype=torch.float32, device=device)
     _dev(out, "out", torch.bfloat16)
     _dev(lse, "lse", torch.float32)
+    if tuple(out.shape) != (rows, H, D_V):
+        raise ValueError(f"out must be [{rows}, {H}, {D_V}], got {tuple(out.shape)}")
+    if tuple(lse.shape) != (rows, H):
+        raise ValueError(f"lse must be [{rows}, {H}], got {tuple(lse.shape)}")
     return out, lse
 
 
-def _tree_args(tree_parent, tree_bits):
+def _tree_args(tree_parent, tree_bits, B: int, T: int):
+    """Pointers of the tree arguments; the one used must hold B*T entries."""
     if tree_bits is not None:
         _dev(tree_bits, "tree_bits", torch.int64)
+        if tree_bits.numel() != B * T:
+            raise ValueError(f"tree_bits must hold B*T = {B * T} masks")
     elif tree_parent is not None:
         _dev(tree_parent, "tree_parent", torch.int32)
+        if tree_parent.numel() != B * T:
+            raise ValueError(f"tree_parent must hold B*T = {B * T} parents")
     return _ptr(tree_parent), _ptr(tree_bits)
 
 
@@ -208,15 +231,14 @@ def prepare_paged(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: torch.Tensor
     _dev(slot_idx, "slot_idx", torch.int32)
     _dev(kv_indptr, "kv_indptr", torch.int32)
     _dev(prefix_len, "prefix_len", torch.int32)
-    if q.dim() != 3 or q.shape[2] != D_QK or kv_pool.dim() != 2:
-        raise ValueError("q must be [B*T, H, 576] and kv_pool [num_slots, stride]")
+    if kv_pool.dim() != 2:
+        raise ValueError("kv_pool must be [num_slots, stride]")
     B = prefix_len.shape[0]
-    T = q.shape[0] // B
-    H = q.shape[1]
+    T, H = _dims(q, B)
     if workspace is None:
         workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
     out, lse = _outputs(q.shape[0], H, q.device, out, lse)
-    par, bits = _tree_args(tree_parent, tree_bits)
+    par, bits = _tree_args(tree_parent, tree_bits, B, T)
     args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
             _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,
             _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
@@ -257,13 +279,14 @@ def verify_attn_contiguous(q: torch.Tensor, kv_pool: torch.Tensor, kv_start: tor
     _dev(kv_pool, "kv_pool", torch.bfloat16)
     _dev(kv_start, "kv_start", torch.int64)
     _dev(prefix_len, "prefix_len", torch.int32)
+    if kv_pool.dim() != 2:
+        raise ValueError("kv_pool must be [num_slots, stride]")
     B = prefix_len.shape[0]
-    T = q.shape[0] // B
-    H = q.shape[1]
+    T, H = _dims(q, B)
     if workspace is None:
         workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
     out, lse = _outputs(q.shape[0], H, q.device, out, lse)
-    par, bits = _tree_args(tree_parent, tree_bits)
+    par, bits = _tree_args(tree_parent, tree_bits, B, T)
     rc = load().verify_attn_contiguous(
         _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_start),
         _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags, _ptr(workspace),
@@ -293,11 +316,10 @@ def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: to
     _dev(kv_indices, "kv_indices", torch.int32)
     _dev(kv_indptr, "kv_indptr", torch.int32)
     _dev(out_cache_loc, "out_cache_loc", torch.int32)
-    if q.dim() != 3 or q.shape[2] != D_QK or kv_pool.dim() != 2:
-        raise ValueError("q must be [B*T, H, 576] and kv_pool [num_slots, stride]")
+    if kv_pool.dim() != 2:
+        raise ValueError("kv_pool must be [num_slots, stride]")
     B = kv_indptr.shape[0] - 1
-    T = q.shape[0] // B
-    H = q.shape[1]
+    T, H = _dims(q, B)
     if out_cache_loc.numel() != B * T:
         raise ValueError("out_cache_loc must hold B*T slots")
     mask_ptr, mask_len = None, 0
@@ -313,7 +335,7 @@ def verify_attn_segmented(q: torch.Tensor, kv_pool: torch.Tensor, kv_indices: to
     if workspace is None:
         workspace, nsplit = alloc_workspace(B, T, H, nsplit, flags, q.device)
     out, lse = _outputs(q.shape[0], H, q.device, out, lse)
-    par, bits = _tree_args(tree_parent, tree_bits)
+    par, bits = _tree_args(tree_parent, tree_bits, B, T)
     rc = load().verify_attn_segmented(
         _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_indices),
         _ptr(kv_indptr), _ptr(out_cache_loc), _ptr(draft_kv), mask_ptr, mask_len, par, bits,
@@ -428,10 +450,12 @@ def verify_attn_paged_noalloc(q: torch.Tensor, kv_pool: torch.Tensor, slot_idx: 
                      (prefix_len, "prefix_len", torch.int32), (out, "out", torch.bfloat16),
                      (lse, "lse", torch.float32)):
         _dev(t, n, dt)
+    if kv_pool.dim() != 2:
+        raise ValueError("kv_pool must be [num_slots, stride]")
     B = prefix_len.shape[0]
-    T = q.shape[0] // B
-    H = q.shape[1]
-    par, bits = _tree_args(tree_parent, tree_bits)
+    T, H = _dims(q, B)
+    _outputs(q.shape[0], H, q.device, out, lse)
+    par, bits = _tree_args(tree_parent, tree_bits, B, T)
     rc = load().verify_attn_paged_noalloc(
         _ptr(q), _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(slot_idx),
         _ptr(kv_indptr), _ptr(prefix_len), par, bits, B, T, H, float(sm_scale), nsplit, flags,

@@ -45,9 +45,9 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
 // kBuf splits per warp in flight) -- they do not depend on the weights, so
 // their round trip to memory overlaps the one of the lse values.  The split
 // weights exp(lse_s - lse) are formed once per CTA in shared memory; each warp
-// then sums its splits and the eight partial sums are added.  Loads of splits
-// past the request's effective split count (slots the split-K kernel did not
-// write) are never used: their terms are selected out, not multiplied by 0.
+// then sums its splits and the eight partial sums are added.  Only the
+// request's effective splits are loaded: slots past them were not written by
+// this call (they may hold an earlier call's data) and are never read.
 constexpr int kBuf = 10;   // splits per warp per round (80 per CTA)
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
@@ -58,12 +58,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   __shared__ float wsplit[kMaxSplits];
   __shared__ float red[kCombineThreads / 32];
   __shared__ float4 part[kCombineThreads / 32][kCombineCols / 4];
-  griddep_wait();   // the split-K kernel's partials are complete and visible
   const int rows_total = p.B * p.rows_per_req;
   const int row = blockIdx.x, chunk = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = row / p.rows_per_req;
   constexpr int kWarps = kCombineThreads / 32;
+  // The request's split count comes from its bounds, which are inputs of the
+  // call rather than results of the split-K kernel (that kernel began after
+  // the stream's earlier work had completed), so they are read before the
+  // wait; only the splits that ran are loaded below.
+  const ReqInfo ri = req_info(p, b, false);
+  const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
+  griddep_wait();   // the split-K kernel's partials are complete and visible
   const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
   const size_t sstride = size_t(rows_total) * kDv;
 
@@ -72,12 +78,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 #pragma unroll
   for (int i = 0; i < kBuf; ++i) {
     const int s = warp + kWarps * i;
-    buf[i] = s < p.nsplit ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
-                          : make_uint2(0u, 0u);
+    buf[i] = s < ne ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
+                    : make_uint2(0u, 0u);
   }
 
-  const ReqInfo ri = req_info(p, b, false);
-  const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
   const float* pl = p.part_lse + row;
   float m = -INFINITY;
   for (int s = tid; s < ne; s += kCombineThreads) {

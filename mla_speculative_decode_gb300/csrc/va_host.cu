@@ -170,7 +170,22 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
 // the symbol itself to a kernel (on the host it names a host-side stand-in);
 // it passes the device address from cudaGetSymbolAddress instead.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[VA_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_ptr[kMaxDevices];   // device address per device, set on first use
+void* g_noalloc_ptr[kMaxDevices];   // device address per device (va_init, else first use)
+
+// Resolves the scratch array's device address on the current device.  This
+// translation unit is a module of its own (no relocatable device code), and
+// under lazy module loading the driver loads a module -- and places its
+// device arrays in memory -- on first use, so this call is where the array's
+// memory is claimed.  va_init makes it, so that the array is in place before
+// a caller reserves the rest of device memory or begins a stream capture.
+cudaError_t resolve_noalloc(int dev) {
+  if (g_noalloc_ptr[dev]) return cudaSuccess;
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) return e != cudaSuccess ? e : cudaErrorUnknown;
+  g_noalloc_ptr[dev] = ptr;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -187,6 +202,10 @@ VA_API int va_init(int device) {
   cudaError_t e1 = va::init_partial_fma();
   int pairs = 0;
   cudaError_t e2 = va::init_partial_tc(&pairs);
+  // the no-allocation scratch array: placed now, with the device current; a
+  // failure here (no memory left for it) is not an error of va_init -- the
+  // first verify_attn_paged_noalloc call on the device retries and reports it
+  if (resolve_noalloc(device) != cudaSuccess) (void)cudaGetLastError();
   cudaSetDevice(prev);
   if (e1 != cudaSuccess || e2 != cudaSuccess) return VA_ERR_CUDA;
   g_dev[device].num_sms = prop.multiProcessorCount;
@@ -293,12 +312,9 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
   DeviceState ds;
   int rc = current_state(&ds);
   if (rc != VA_OK) return rc;
-  if (!g_noalloc_ptr[dev]) {
-    // first call on this device: resolve the array's device address once
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return VA_ERR_CUDA;
-    g_noalloc_ptr[dev] = ptr;
-  }
+  // normally resolved by va_init; otherwise (va_init could not place the
+  // array) this first call on the device tries again
+  if (!g_noalloc_ptr[dev] && resolve_noalloc(dev) != cudaSuccess) return VA_ERR_CUDA;
   int ns = nsplit;
   if (ns == 0) {
     const int path = pick_path(flags, B, T, H);

@@ -124,18 +124,83 @@ def test_forced_rescales(va, path, nsplit):
     _gpu.compare(out, lse, ref_o, ref_l)
 
 
-# -------------------------------------------- full sizes, sampled rows
+# -------------------------------------------- full sizes
 
-@pytest.mark.parametrize("name", ["fullh", "long", "batched"])
+@pytest.mark.parametrize("layout", ["scattered", "contiguous"])
+def test_fullh_every_row(va, layout):
+    """The full-H configuration (H=64, T=16, prefix 65536: eight 128-row
+    blocks), in both layouts the benchmark times -- scattered slots and the
+    contiguous (defragmented) pool read by 3-D TMA boxes -- at the automatic
+    split count, compared with the oracle on every one of its 1024 rows."""
+    w = synth.make(synth.spec("fullh", layout=layout))
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=0)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name", ["long", "batched"])
 def test_full_size_sampled_rows(va, name):
-    """The large configurations at the benchmark's launch setting (automatic
-    split count), checked on sampled rows the oracle evaluates one by one."""
+    """The long-context and batched configurations at the benchmark's launch
+    setting (automatic split count), checked on sampled rows the oracle
+    evaluates one by one."""
     w = synth.make(synth.spec(name))
     d = _gpu.to_device(w)
     out, lse = _gpu.run(va, d, w, path=0)
-    rows = _gpu.sample_rows(w, 48, seed=1)
+    rows = _gpu.sample_rows(w, 256 if name == "long" else 512, seed=1)
     ref_o, ref_l = _gpu.reference(w, rows=rows)
     _gpu.compare(out, lse, ref_o, ref_l, rows=rows)
+
+
+def test_batched_replayed_graph_with_new_prefixes_and_slots(va):
+    """The batched configuration (8 requests, H=64, T=16, ragged prefixes in
+    [1024, 65536], one shared 2^20-slot pool) captured into a CUDA graph once
+    and replayed: first on its own inputs, then after new prefix lengths, slot
+    tables, trees and queries of another draw were copied into the same
+    buffers.  Each replay is compared with the oracle on sampled rows and with
+    an eager call on the same inputs bit for bit."""
+    s1 = synth.spec("batched")
+    g = torch.Generator().manual_seed(4242)
+    pre2 = [int(x) for x in torch.randint(1024, 65537, (s1.B,), generator=g)]
+    s2 = synth.spec("batched", prefix=pre2, seed=14)
+    w1 = synth.make(s1)
+    w2 = synth.make(s2)
+    w2.kv_pool = w1.kv_pool
+    d = _gpu.to_device(w1)
+    cap = max(w1.slot_idx.numel(), w2.slot_idx.numel())
+    slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    slots[:w1.slot_idx.numel()] = d["slot_idx"]
+    d["slot_idx"] = slots
+    ws, ns = va.alloc_workspace(s1.B, s1.T, s1.H)
+    rows_total = s1.B * s1.T
+    out = torch.empty(rows_total, s1.H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(rows_total, s1.H, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        _gpu.run(va, d, w1, nsplit=ns, workspace=ws, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _gpu.run(va, d, w1, nsplit=ns, workspace=ws, out=out, lse=lse)
+    for w, seed in ((w1, 11), (w2, 12)):
+        if w is w2:
+            d["q"].copy_(w2.q.cuda())
+            d["slot_idx"][:w2.slot_idx.numel()].copy_(w2.slot_idx.cuda())
+            d["kv_indptr"].copy_(w2.kv_indptr.cuda())
+            d["prefix_len"].copy_(w2.prefix_len.cuda())
+            d["parents"].copy_(w2.parents.cuda())
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert va.read_status(ws) == 0
+        o_rep, l_rep = out.clone(), lse.clone()
+        o_eager, l_eager = _gpu.run(va, d, w, nsplit=ns)
+        torch.cuda.synchronize()
+        assert torch.equal(o_rep, o_eager) and torch.equal(l_rep, l_eager)
+        rows = _gpu.sample_rows(w, 256, seed=seed)
+        ref_o, ref_l = _gpu.reference(w, rows=rows)
+        _gpu.compare(o_rep, l_rep, ref_o, ref_l, rows=rows)
 
 
 def test_long_nsplit_sweep(va):
@@ -161,6 +226,27 @@ def test_contiguous_matches_oracle_and_paged(va, path):
     d = _gpu.to_device(w)
     out_c, lse_c = _gpu.run(va, d, w, path=path, layout="contiguous", nsplit=8)
     out_p, lse_p = _gpu.run(va, d, w, path=path, layout="scattered", nsplit=8)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out_c, lse_c, ref_o, ref_l)
+    assert torch.equal(out_c, out_p) and torch.equal(lse_c, lse_p)
+
+
+@pytest.mark.parametrize("nsplit", [0, 3, 11])
+def test_contiguous_full_h_row_blocks(va, nsplit):
+    """Contiguous pools at H=64, T=16 (eight 128-row blocks per request): the
+    whole 64-key tiles arrive as one 3-D TMA box, each split's ragged last tile
+    by 16-byte copies; two requests with different prefix lengths (neither a
+    multiple of 64).  Every row against the oracle, and bit for bit against the
+    paged call on the same rows."""
+    s = synth.Spec("contig_h64", B=2, H=64, T=16, prefix=[3000, 1237], num_slots=1 << 14,
+                   layout="contiguous", seed=37)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H, nsplit)
+    out_c, lse_c = _gpu.run(va, d, w, layout="contiguous", nsplit=ns, workspace=ws)
+    assert va.read_status(ws) == 0
+    out_c, lse_c = out_c.clone(), lse_c.clone()
+    out_p, lse_p = _gpu.run(va, d, w, layout="scattered", nsplit=ns)
     ref_o, ref_l = _gpu.reference(w)
     _gpu.compare(out_c, lse_c, ref_o, ref_l)
     assert torch.equal(out_c, out_p) and torch.equal(lse_c, lse_p)
