@@ -74,9 +74,14 @@ constexpr uint32_t kBlockBytes = kTile * 128;               // 8 KB: 64 keys x 6
 // of shared memory per 128 cycles, a 128-wide one 8 KB per 64 cycles, more
 // than the shared memory can deliver next to the incoming copies.
 constexpr int kRingK = 23;
-constexpr int kRingV = 16;
+constexpr int kRingV = 20;
 constexpr int kVGroup = 4;                                  // value blocks per PV product
 static_assert(kRingV % kVGroup == 0 && kRingK >= 2 * kKBlocks && kRingV >= 2 * kVBlocks, "rings");
+// Key tile t occupies ring positions [9t, 9t + 9) mod kRingK, last held by
+// blocks 4-8 of tile t-3 and blocks 0..kKRelease of tile t-2: the products
+// commit once those blocks of a tile are read.
+constexpr int kKRelease = kKBlocks - 1 - (kRingK - 2 * kKBlocks);
+static_assert(kKRelease >= 0 && kKRelease < kKBlocks && kRingK < 3 * kKBlocks, "key ring reuse");
 // P buffer: P tile (128 rows x 64 keys bf16, K-major 128B swizzle), then the
 // rows' rescale factors, then the four softmax warps' rescale flags.  Shipped
 // to the PV CTA as one contiguous bulk copy.
@@ -85,7 +90,7 @@ constexpr uint32_t kPAlpha = kPBytes;                       // float [128]
 constexpr uint32_t kPFlags = kPAlpha + 4 * kRows;           // uint32 [4]
 constexpr uint32_t kPPayload = kPFlags + 16;                // bytes copied
 constexpr uint32_t kPBufBytes = 17 * 1024;                  // buffer stride (1024-aligned)
-constexpr int kPBufs = 4;                                   // P ring depth (PV CTA)
+constexpr int kPBufs = 3;                                   // P ring depth (PV CTA)
 constexpr int kValidRing = 8;
 constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
 
@@ -93,7 +98,8 @@ constexpr uint32_t kCmdDone = 0xFFFFFFFFu;
 // arrivals and multicast commits land on the right objects.
 enum : int {
   B_FULL = 0,                 // [2] tile landed (K in the QK CTA, V in the PV CTA)
-  B_EMPTY = 2,                // [kRingK] slot released by the MMAs that read it
+  B_EMPTY = 2,                // [kRingK] PV CTA: value slot released by the MMAs that read
+                              // it; QK CTA: [2] key slots of tile t released (t % 2)
   B_SFULL = B_EMPTY + kRingK, // [2]
   B_SEMPTY = B_SFULL + 2,     // [2]
   B_PFREE = B_SEMPTY + 2,     // [kPBufs] (QK CTA; committed by the PV CTA)
@@ -197,7 +203,8 @@ __device__ __forceinline__ int checked_row(const Params& p, int raw) {
 //    (64 columns x 64 rows x nb column blocks, map `map3`) lands the whole
 //    tile; otherwise one 64 x 64 box per column block (2-D map `map2`).
 // Before filling a tile, producer 0 waits for the release of its slots by the
-// products of the tiles that used them before.  With kMask the
+// products of the tiles that used them before (value side: the slot of the
+// tile's last block; key side: blocks 0-3 of the tile two back).  With kMask the
 // tile's 64-bit key-validity mask goes to the ring read by the softmax warps.
 // Completion: every producer's cp.async arrival (noinc) on the tile's full
 // barrier plus one arrival of producer 0 (carrying the TMA byte count when
@@ -228,13 +235,23 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     // per tile: each one costs a wake-up latency, and nine in a row cost more
     // than the deeper ring gains.)  The others learn the outcome at the named
     // barrier below.
-    {
+    if (kMask) {
+      // QK side: tile t's slots last held blocks of tile t-3 and blocks
+      // 0..kKRelease of tile t-2; the products commit once when a tile's
+      // blocks 0..kKRelease are read (barrier t % 2), so one wait covers them
+      // all.  (Each commit
+      // costs the issuing warp about as much as an N=64 product, so the QK
+      // products commit twice per tile, not once per slot.)  Tile 1's slots
+      // hold Q until its rows are in TMEM.
+      if (ptid == 0 && t >= 2)
+        got = mbar_wait(empty0 + 8u * uint32_t(t & 1), uint32_t((t - 2) >> 1) & 1u, abort_flag,
+                        kWaitCycles);
+      if (ptid == 0 && t == 1) got = mbar_wait(qready, 0, abort_flag, kWaitCycles);
+    } else {
       const int g = g0 + kBlocks - 1;
       if (ptid == 0 && g >= kRing)
         got = mbar_wait(empty0 + 8u * uint32_t(g % kRing), uint32_t(g / kRing - 1) & 1u, abort_flag,
                         kWaitCycles);
-      // QK side: tile 1's slots hold Q until its rows are in TMEM
-      if (kMask && ptid == 0 && t == 1) got = mbar_wait(qready, 0, abort_flag, kWaitCycles);
     }
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 0, t);
     VA_PH(0);
@@ -466,8 +483,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + kTmemS + 64u * uint32_t(bs);
         // K columns 16k..16k+15 (k = 4c + kk): column block c in its ring
         // slot, 32-byte step kk inside the swizzled row (the descriptor's
-        // address field counts 16-byte units); each slot is released as soon
-        // as its four products complete
+        // address field counts 16-byte units).  Two commits per tile: blocks
+        // 0..kKRelease read (the producers refill the tile's slots two tiles
+        // on), then the
+        // whole tile (S ready, every slot read).  A commit costs an N=64
+        // product's issue slot (measured: 45 cycles per product with a commit
+        // after every fourth, 34.5 without), so the slots are not released
+        // one by one.
 #pragma unroll
         for (int c = 0; c < kKBlocks; ++c) {
           const int sl = s0 + c < kRingK ? s0 + c : s0 + c - kRingK;
@@ -477,7 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             mma_ts_warp(d, tmem + kTmemQ + 8u * uint32_t(4 * c + kk),
                         bd + uint64_t((uint32_t(kk) * 32u) >> 4), idesc, (c | kk) != 0 ? 1u : 0u);
-          mma_commit_warp(bar(B_EMPTY + sl));
+          if (c == kKRelease) mma_commit_warp(bar(B_EMPTY + bs));
         }
         mma_commit_warp(bar(B_SFULL + bs));
         if (lane == 0) VA_TRACE_EVENT(1, 1, t);
