@@ -1,14 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark of one MLA tree-verify attention step on GB300.
 
-Default workload: one request, H=8 heads, T=16 random draft-tree nodes,
-prefix 4096 keys, bf16 latent KV gathered through a page_size=1 slot table
-scattered over a 2^20-slot pool (the TP8 slice).  A step is one verify call:
-tree-mask evaluation, split-K partial attention and the LSE merge.
+Headline workload (the largest one-GPU configuration): the batched ragged
+step -- 8 requests, H=64 heads, T=16 random draft-tree nodes each, prefixes
+drawn uniformly from [1024, 65536], bf16 latent KV gathered through a
+page_size=1 slot table scattered over one shared 2^20-slot pool, steps
+captured and replayed in CUDA graphs.  A step is one verify call: split-K
+partial attention (tree masks computed inside) and the LSE merge.
 
 Prints ONE JSON line: effective KV GB/s (whole job), us/step, the split-K
-kernel's roofline fraction, the oracle timed on the host cores, an
-end-to-end figure through the C ABI with host buffers, clocks and launches.
+kernel's roofline fraction (tensor-bound at H=64), the target points (H=8 and
+H=64 at prefixes 16k, 65k and 200k, scattered and contiguous) with their
+kernel-level fractions, the oracle timed on the host cores, an end-to-end
+figure through the C ABI with host buffers, clocks and launches.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -32,26 +36,39 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "verify-attn µs/step and effective KV GB/s (% of HBM roofline) vs prefix length"
-WORKLOAD = ("TP8 slice: 1 request, H=8, T=16 random tree, prefix 4096, bf16 latent KV "
-            "(576 = 512 + 64), page_size=1 slots scattered over a 2^20-slot pool, "
-            "sm_scale=1/sqrt(192)")
-SWEEP_P = [4096, 16384, 32768, 65536, 131072, 200000]
+HEADLINE = "batched"
+WORKLOAD = ("batched ragged: 8 requests, H=64, T=16 random trees, prefixes U[1024, 65536] "
+            "(seeded: 14817, 40180, 26978, 43472, 28365, 46466, 13339, 17238), bf16 latent KV "
+            "(576 = 512 + 64), page_size=1 slots scattered over one shared 2^20-slot pool, "
+            "sm_scale=1/sqrt(192), captured and replayed in CUDA graphs")
+TARGET_P = [16384, 65536, 200000]
+SWEEP_P = [4096, 32768, 131072]
+
+
+def headline_config(step=None) -> dict:
+    """The `config` object of both arms' lines (the same dict, so the two
+    describe one workload)."""
+    s = synth.spec(HEADLINE)
+    cfg = {"workload": WORKLOAD, "B": s.B, "H": s.H, "T": s.T, "prefix": list(s.prefix),
+           "layout": "scattered", "pool_slots": s.num_slots,
+           "kv_bytes_per_step": s.kv_bytes()}
+    return cfg
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 FMA, 2 tensor cores")
     ap.add_argument("--nsplit", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--case", default="",
-                    help="H,prefix,layout: run only --warmup + --steps plain calls of that "
-                         "workload (the small captures the ncu summaries are made from); "
-                         "prints a timing note, not the benchmark line")
+                    help="'batched' or H,prefix,layout[,T]: run only --warmup + --steps plain "
+                         "calls of that workload (the captures the ncu summaries are made "
+                         "from); prints a timing note, not the benchmark line")
     return ap.parse_args()
 
 
@@ -83,15 +100,25 @@ def recorded_traffic():
 
 
 def run_case(va, args, dev):
-    """A few plain verify calls of one workload, for profiler captures."""
-    H, P, layout = args.case.split(",")
-    H, P = int(H), int(P)
-    rows = 1 << 18
-    while rows < 2 * (P + 16):
-        rows *= 2
-    pool = device_pool(rows, seed=1, dev=dev)
-    st = Step(va, pool, H, 16, P, seed=7, nrot=2, dev=dev, path=args.path, nsplit=args.nsplit,
-              layout=layout)
+    """A few plain verify calls of one workload, for profiler captures:
+    `--case batched` (the headline step) or `--case H,prefix,layout[,T]`."""
+    if args.case == HEADLINE:
+        s = synth.spec(HEADLINE)
+        pool = device_pool(s.num_slots, seed=1, dev=dev)
+        st = Step(va, pool, s.H, s.T, list(s.prefix), seed=4, nrot=2, dev=dev, path=args.path,
+                  nsplit=args.nsplit)
+        label = HEADLINE
+    else:
+        parts = args.case.split(",")
+        H, P, layout = int(parts[0]), int(parts[1]), parts[2]
+        T = int(parts[3]) if len(parts) > 3 else 16
+        rows = 1 << 18
+        while rows < 2 * (P + T):
+            rows *= 2
+        pool = device_pool(rows, seed=1, dev=dev)
+        st = Step(va, pool, H, T, P, seed=7, nrot=2, dev=dev, path=args.path, nsplit=args.nsplit,
+                  layout=layout)
+        label = f"H={H} T={T} P={P} {layout}"
     for k in range(args.warmup):
         st.call(k)
     torch.cuda.synchronize()
@@ -102,7 +129,7 @@ def run_case(va, args, dev):
     b.record()
     torch.cuda.synchronize()
     us = a.elapsed_time(b) / max(1, args.steps) * 1e3
-    print(f"case H={H} P={P} {layout} nsplit={st.nsplit}: {us:.2f} us/call "
+    print(f"case {label} nsplit={st.nsplit}: {us:.2f} us/call "
           f"(eager launches, not the benchmark figure)", flush=True)
 
 
@@ -275,9 +302,30 @@ class Step:
             # the draft tokens' new latents, written into their slots by the call
             self.draft = ((torch.randn(B * T, synth.D_QK, generator=g)).to(torch.bfloat16).to(dev)
                           if layout == "segmented_append" else None)
+        self.prefixes = prefixes
+        self.offs = offs
         self.kv_bytes = self.N * synth.D_QK * 2
-        # tensor-core work: 2176 flop (2*576 + 2*512) for every row and every key
-        self.flops = sum(2176.0 * T * H * n for n in Ns)
+        # algorithmic tensor work: 2176 flop (2*576 + 2*512) per visible
+        # (row, key) pair -- every prefix key, plus each node's ancestors and
+        # itself among the draft keys
+        par = self.parents.cpu().tolist()
+        pairs = 0
+        for b in range(B):
+            for i in range(T):
+                k, depth = i, 0
+                while 0 <= k < T:
+                    depth += 1
+                    k = par[b][k] if par[b][k] < k else -1
+                pairs += H * (prefixes[b] + depth)
+        self.visible_pairs = pairs
+        self.flops = 2176.0 * pairs
+
+    def table_rows(self, k: int) -> torch.Tensor:
+        """Pool rows (int64) of rotation k's keys, requests one after the other."""
+        if self.layout == "contiguous":
+            return torch.arange(k % self.nrot * self.N, (k % self.nrot + 1) * self.N,
+                                dtype=torch.int64, device=self.pool.device)
+        return self.tables[k % self.nrot].long()
 
     def call(self, k, stream=None):
         if self.layout in ("segmented", "segmented_append"):
@@ -303,10 +351,12 @@ class Step:
 STEPS_PER_GRAPH = 8
 
 
-def capture_graphs(step: Step, with_events: bool, per_graph: int = 1):
-    """CUDA graphs over the rotated slot tables, `per_graph` consecutive steps
-    (each on its own table) per graph; with events, one step per graph and
-    event records around its split-K kernel."""
+def capture_graphs(step: Step, K: int, with_events: bool = False):
+    """CUDA graphs over the rotated slot tables: graphs of STEPS_PER_GRAPH
+    consecutive steps (each on its own table), as a serving loop would capture
+    them, and -- when K is not a multiple of that -- one graph of the K % 8
+    remaining steps, so that exactly K steps can be replayed.  With events:
+    one-step graphs with event records around the split-K kernel instead."""
     va = step.va
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -315,29 +365,50 @@ def capture_graphs(step: Step, with_events: bool, per_graph: int = 1):
             step.call(k)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    graphs, evs = [], []
-    per_graph = 1 if with_events else max(1, per_graph)
-    ngraphs = max(1, step.nrot // per_graph)
-    for gi in range(ngraphs):
-        g = torch.cuda.CUDAGraph()
-        if with_events:
+    if with_events:
+        graphs, evs = [], []
+        for gi in range(min(step.nrot, 8)):
+            g = torch.cuda.CUDAGraph()
             eb = torch.cuda.Event(enable_timing=True)
             ea = torch.cuda.Event(enable_timing=True)
             va.set_partial_events(eb, ea)
             evs.append((eb, ea))
+            with torch.cuda.graph(g):
+                step.call(gi)
+            graphs.append(g)
+        va.set_partial_events(None, None)
+        return graphs, evs
+    per = STEPS_PER_GRAPH
+    full = []
+    for gi in range(max(1, step.nrot // per)):
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for j in range(per_graph):
-                step.call(gi * per_graph + j)
-        graphs.append(g)
-    va.set_partial_events(None, None)
-    return graphs, evs
+            for j in range(per):
+                step.call(gi * per + j)
+        full.append(g)
+    tail = None
+    if K % per:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail):
+            for j in range(K % per):
+                step.call(j)
+    return (full, tail), None
 
 
-def time_graphs(graphs, K, W, dist=None, per_graph: int = 1):
-    """Times exactly K steps: K / per_graph replays (K a multiple of per_graph)."""
-    assert K % per_graph == 0 and W >= 1
-    for k in range(max(1, -(-W // per_graph))):
-        graphs[k % len(graphs)].replay()
+def replay_steps(graphs, K: int):
+    """Replays exactly K steps: K // 8 eight-step graphs, then the tail graph."""
+    full, tail = graphs
+    for r in range(K // STEPS_PER_GRAPH):
+        full[r % len(full)].replay()
+    if K % STEPS_PER_GRAPH:
+        tail.replay()
+
+
+def time_steps(graphs, K: int, W: int, dist=None) -> float:
+    """ms for exactly K timed steps after at least W warm-up steps; barrier and
+    device synchronisation on both sides of the timed region."""
+    assert W >= 1
+    replay_steps(graphs, -(-W // STEPS_PER_GRAPH) * STEPS_PER_GRAPH)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -345,8 +416,7 @@ def time_graphs(graphs, K, W, dist=None, per_graph: int = 1):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for k in range(K // per_graph):
-        graphs[k % len(graphs)].replay()
+    replay_steps(graphs, K)
     e1.record()
     torch.cuda.synchronize()
     if dist is not None:
@@ -355,122 +425,160 @@ def time_graphs(graphs, K, W, dist=None, per_graph: int = 1):
     return e0.elapsed_time(e1)
 
 
-def kernel_ms(evs, used):
-    """Average split-K kernel duration over the last replay of each graph used."""
-    n = min(len(evs), used)
-    return float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in range(n)]))
+def partial_kernel_us(step: Step) -> float:
+    """Average duration of the split-K kernel (CUDA events recorded by the
+    library on the launching stream around it), over one-step graphs replayed
+    twice after the timed region."""
+    egraphs, evs = capture_graphs(step, 1, with_events=True)
+    for _ in range(2):
+        for g in egraphs:
+            g.replay()
+    torch.cuda.synchronize()
+    us = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+    del egraphs
+    return us
 
 
 def measure_dist(step: Step, K: int, W: int, runs: int = 5):
     """Per-step µs of `runs` timed runs of K steps each: (median, p10, p90), and
     the split-K kernel µs."""
-    per = STEPS_PER_GRAPH if K % STEPS_PER_GRAPH == 0 and step.nrot >= STEPS_PER_GRAPH else 1
-    graphs, _ = capture_graphs(step, with_events=False, per_graph=per)
-    egraphs, evs = capture_graphs(step, with_events=True)
-    vals = [time_graphs(graphs, K, W if i == 0 else 1, None, per_graph=per) / K * 1e3
-            for i in range(runs)]
-    for g in egraphs:
-        g.replay()
-    for g in egraphs:
-        g.replay()
-    torch.cuda.synchronize()
-    k_us = kernel_ms(evs, len(egraphs)) * 1e3
-    del graphs, egraphs
+    graphs, _ = capture_graphs(step, K)
+    vals = [time_steps(graphs, K, W if i == 0 else 1) / K * 1e3 for i in range(runs)]
+    del graphs
+    k_us = partial_kernel_us(step)
     v = np.array(vals)
     return float(np.median(v)), float(np.percentile(v, 10)), float(np.percentile(v, 90)), k_us
 
 
-def measure(step: Step, K: int, W: int, dist=None):
-    """(ms for K steps, ms of the split-K kernel).  The step time comes from
-    graphs with nothing but the steps' kernels -- eight consecutive steps, each
-    on its own rotated slot table, per graph, as a serving loop would capture
-    them, so that host-side graph submission does not pace the device -- and
-    each kernel may start while its predecessor finishes (programmatic
-    dependent launch); the kernel time from a second set of one-step graphs
-    with event records around the split-K kernel, replayed after the timed
-    region."""
-    per = STEPS_PER_GRAPH if K % STEPS_PER_GRAPH == 0 and step.nrot >= STEPS_PER_GRAPH else 1
-    graphs, _ = capture_graphs(step, with_events=False, per_graph=per)
-    egraphs, evs = capture_graphs(step, with_events=True)
-    ms = time_graphs(graphs, K, W, dist, per_graph=per)
-    for g in egraphs:
-        g.replay()
-    for g in egraphs:
-        g.replay()
-    torch.cuda.synchronize()
-    k_ms = kernel_ms(evs, len(egraphs))
-    del graphs, egraphs
-    return ms, k_ms
-
-
-def check_parity(step: Step, k: int, nrows: int = 8):
-    """Sampled rows of step k against the fp64 oracle (compact copy of the rows used)."""
-    import oracle
-    step.call(k)
-    torch.cuda.synchronize()
-    table = step.tables[k % step.nrot].long()
-    rows_kv = step.pool[table].cpu()
-    rng = np.random.default_rng(k)
-    rows = np.sort(rng.choice(step.T * step.H, size=min(nrows, step.T * step.H), replace=False))
-    bits, _ = oracle.tree_bits(step.parents.cpu().numpy())
-    ro, rl, _ = oracle.verify_attn(synth.as_u16(step.q.cpu()), synth.as_u16(rows_kv),
-                                   np.arange(step.N, dtype=np.int32), np.array([0, step.N]),
-                                   np.array([step.P]), bits, synth.SM_SCALE, rows=rows)
-    go = step.out.float().reshape(-1, 512).cpu().numpy()[rows]
-    gl = step.lse.reshape(-1).cpu().numpy()[rows]
-    err = float(np.abs(go - ro).max())
-    mean = float(np.abs(go - ro).mean())
-    lerr = float(np.abs(gl - rl).max())
-    return {"rows": int(len(rows)), "max_abs": err, "mean_abs": mean, "lse_max_abs": lerr,
-            "ok": bool(err <= 2e-2 and mean <= 2e-3 and lerr <= 1e-3)}
+def point_record(step: Step, us: float, p10: float, p90: float, k_us: float, hbm_peak: float,
+                 tc_peak: float) -> dict:
+    """One measured point: step and split-K kernel figures against both roofs."""
+    kvb = step.kv_bytes
+    return {"us_per_step": us, "p10": p10, "p90": p90,
+            "gbs": kvb / (us * 1e-6) / 1e9, "frac_hbm": kvb / (us * 1e-6) / 1e9 / hbm_peak,
+            "tflops": step.flops / (us * 1e-6) / 1e12,
+            "frac_tensor": step.flops / (us * 1e-6) / 1e12 / tc_peak,
+            "kernel_us": k_us, "kernel_gbs": kvb / (k_us * 1e-6) / 1e9,
+            "kernel_frac_hbm": kvb / (k_us * 1e-6) / 1e9 / hbm_peak,
+            "kernel_tflops": step.flops / (k_us * 1e-6) / 1e12,
+            "kernel_frac_tensor": step.flops / (k_us * 1e-6) / 1e12 / tc_peak,
+            "nsplit": step.nsplit, "kv_bytes": kvb, "flops": step.flops}
 
 
 # --------------------------------------------------------------- oracle
 
-def cpu_oracle(P, H, T, seed, budget_s=12.0, threads=None):
-    """The fp64 oracle on whole steps of the same workload until ~budget_s."""
-    import oracle
-    threads = threads or oracle.default_threads()
-    g = torch.Generator().manual_seed(seed)
-    N = P + T
-    q = synth.as_u16(torch.randn(T, H, synth.D_QK, generator=g).to(torch.bfloat16))
-    kv = synth.as_u16(torch.randn(N, synth.D_QK, generator=g).to(torch.bfloat16))
-    parents = synth.make_parents(T, "random", g).view(1, T).numpy()
-    bits, _ = oracle.tree_bits(parents)
-    slots = np.random.default_rng(seed).permutation(N).astype(np.int32)
-    t0 = time.perf_counter()
-    steps = 0
-    while True:
-        oracle.verify_attn(q, kv, slots, np.array([0, N]), np.array([P]), bits, synth.SM_SCALE,
-                           threads=threads)
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or steps >= 1000:
+def sample_rows_by_work(step: Step, budget_pairs: float, seed: int):
+    """Query rows of a step sampled at random until their visible (row, key)
+    pairs reach `budget_pairs`; returns (rows, fraction of the step's pairs)."""
+    par = step.parents.cpu().tolist()
+    rows_total = step.B * step.T * step.H
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(rows_total)
+    got, pairs = [], 0
+    for r in order:
+        b, i = divmod(int(r) // step.H, step.T)
+        k, depth = i, 0
+        while 0 <= k < step.T:
+            depth += 1
+            k = par[b][k] if par[b][k] < k else -1
+        got.append(int(r))
+        pairs += step.prefixes[b] + depth
+        if pairs >= budget_pairs:
             break
-    per = el / steps
-    return {"value": N * synth.D_QK * 2 / per / 1e9, "unit": "GB/s", "cores": int(threads),
-            "kind": "oracle", "us_per_step": per * 1e6,
-            "sample": f"{steps} whole step(s) of the same shape (P={P}, H={H}, T={T}), "
-                      f"fp64, {el:.1f} s"}
+    return np.sort(np.array(got, dtype=np.int64)), pairs / step.visible_pairs
+
+
+def oracle_inputs(step: Step, k: int):
+    """Host copies of step k's inputs for the oracle: the queries, the rows the
+    step reads (compacted, in slot-table order), the bounds and the masks."""
+    import oracle
+    rows_kv = step.pool[step.table_rows(k)].cpu()
+    bits, _ = oracle.tree_bits(step.parents.cpu().numpy())
+    return (synth.as_u16(step.q.cpu()), synth.as_u16(rows_kv), np.arange(step.N, dtype=np.int32),
+            np.array(step.offs, dtype=np.int64), np.array(step.prefixes, dtype=np.int64), bits)
+
+
+def cpu_baseline_leg(step: Step, budget_s: float = 12.0, threads=None):
+    """The fp64 oracle, as it stands, on the host cores: a bounded sample of
+    rows of step 0 of the headline workload (about `budget_s` of work), scaled
+    to the metric by the sample's share of the step's visible (row, key)
+    pairs.  The same rows of the GPU's step 0 are compared with it (the
+    parity spot check of the line)."""
+    import oracle
+    oracle.build()
+    threads = threads or oracle.default_threads()
+    step.call(0)
+    torch.cuda.synchronize()
+    go_all = step.out.float().reshape(-1, synth.D_V).cpu().numpy()
+    gl_all = step.lse.reshape(-1).cpu().numpy()
+    q, kv, slots, indptr, prefix, bits = oracle_inputs(step, 0)
+    # calibrate on 1 % of the step's work, then take a sample sized to the
+    # budget (at most the whole step)
+    rows, frac = sample_rows_by_work(step, step.visible_pairs * 0.01, seed=11)
+    t0 = time.perf_counter()
+    oracle.verify_attn(q, kv, slots, indptr, prefix, bits, synth.SM_SCALE, rows=rows,
+                       threads=threads)
+    t_cal = max(time.perf_counter() - t0, 1e-3) / frac      # seconds per whole step
+    share = min(1.0, budget_s / t_cal)
+    rows, frac = sample_rows_by_work(step, step.visible_pairs * share, seed=12)
+    t0 = time.perf_counter()
+    ro, rl, _ = oracle.verify_attn(q, kv, slots, indptr, prefix, bits, synth.SM_SCALE, rows=rows,
+                                   threads=threads)
+    el = time.perf_counter() - t0
+    per_step = el / frac
+    go, gl = go_all[rows], gl_all[rows]
+    err = float(np.abs(go - ro).max())
+    mean = float(np.abs(go - ro).mean())
+    lerr = float(np.abs(gl - rl).max())
+    parity = {"rows": int(len(rows)), "max_abs": err, "mean_abs": mean, "lse_max_abs": lerr,
+              "ok": bool(err <= 2e-2 and mean <= 2e-3 and lerr <= 1e-3)}
+    cpu = {"value": step.kv_bytes / per_step / 1e9, "unit": "GB/s", "cores": int(threads),
+           "kind": "oracle", "us_per_step": per_step * 1e6,
+           "sample": f"{len(rows)} of {step.B * step.T * step.H} query rows of one step "
+                     f"({frac * 100:.2f} % of its visible (row, key) pairs), fp64, {el:.1f} s; "
+                     f"scaled to a whole step by that share"}
+    return cpu, parity
 
 
 def reference_arm(args, rank):
+    """--impl reference: the fp64 oracle on the host cores, on the headline
+    workload; each step a bounded sample of its query rows (the same rows every
+    step), its throughput scaled to a whole step by the sample's share of the
+    visible (row, key) pairs."""
     if rank != 0:
         return
     import oracle
     oracle.build()
     threads = oracle.default_threads()
-    P, H, T = 4096, 8, 16
-    g = torch.Generator().manual_seed(1)
-    N = P + T
-    q = synth.as_u16(torch.randn(T, H, synth.D_QK, generator=g).to(torch.bfloat16))
-    kv = synth.as_u16(torch.randn(N, synth.D_QK, generator=g).to(torch.bfloat16))
-    parents = synth.make_parents(T, "random", g).view(1, T).numpy()
-    slots = np.random.default_rng(1).permutation(N).astype(np.int32)
+    s = synth.spec(HEADLINE)
+    total = sum(s.n_keys())
+    w = synth.make(synth.spec(HEADLINE, num_slots=total))   # a compact pool: the rows used
+    bits, _ = oracle.tree_bits(w.parents.numpy())
+    q, kv = synth.as_u16(w.q), synth.as_u16(w.kv_pool)
+    slots, indptr, prefix = w.slot_idx.numpy(), w.kv_indptr.numpy(), w.prefix_len.numpy()
+    par = w.parents.tolist()
+    pairs_all, row_pairs = 0, []
+    for b in range(s.B):
+        for i in range(s.T):
+            k, depth = i, 0
+            while 0 <= k < s.T:
+                depth += 1
+                k = par[b][k] if par[b][k] < k else -1
+            for _ in range(s.H):
+                row_pairs.append(s.prefix[b] + depth)
+                pairs_all += s.prefix[b] + depth
+    rng = np.random.default_rng(5)
+    rows, got = [], 0
+    for r in rng.permutation(len(row_pairs)):      # about 2 % of the step's work
+        rows.append(int(r))
+        got += row_pairs[r]
+        if got >= pairs_all * 0.02 and len(rows) >= 4 * threads:
+            break
+    rows = np.sort(np.array(rows, dtype=np.int64))
+    frac = got / pairs_all
 
     def one():
-        bits, _ = oracle.tree_bits(parents)
-        oracle.verify_attn(q, kv, slots, np.array([0, N]), np.array([P]), bits, synth.SM_SCALE,
+        oracle.verify_attn(q, kv, slots, indptr, prefix, bits, s.sm_scale, rows=rows,
                            threads=threads)
 
     for _ in range(args.warmup):
@@ -479,21 +587,237 @@ def reference_arm(args, rank):
     for _ in range(args.steps):
         one()
     el = time.perf_counter() - t0
-    ms = el / args.steps * 1e3
-    val = N * synth.D_QK * 2 / (ms / 1e3) / 1e9
+    ms = el / args.steps / frac * 1e3          # per whole step
+    val = s.kv_bytes() / (ms / 1e3) / 1e9
+    sample = (f"each step: {len(rows)} of {s.B * s.T * s.H} query rows ({frac * 100:.3f} % of "
+              f"the visible (row, key) pairs), fp64 on {threads} host threads; scaled to a "
+              f"whole step by that share")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD + " (each step: the whole step on the host cores)"},
+            "config": headline_config(),
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{args.steps} whole steps"},
+                             "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ end to end
+
+def e2e_leg(va, step: Step, K: int, W: int, dist, dev):
+    """The headline metric end to end through the public API with host
+    buffers.  Every step: its inputs (q, slot table, indptr, prefix lengths,
+    parents), packed in one pinned host buffer, are copied to the device with
+    one host-to-device copy; the verify call runs on views of that device
+    buffer; out and lse, views of one device result buffer, are read back with
+    one device-to-host copy into pinned memory.  Two input and two result
+    buffers alternate, and the copies run on their own streams, so step k+1's
+    upload and step k-1's read-back overlap step k's kernels.  Steps are
+    captured eight to a CUDA graph (streams forked and joined inside the
+    capture) and replayed; exactly K steps are timed."""
+    def align(n):
+        return (n + 255) // 256 * 256
+
+    parts = [("q", step.q), ("tab", step.tables[0]), ("par", step.parents),
+             ("ind", step.indptr), ("pre", step.prefix)]
+    offs, o = {}, 0
+    for name, t in parts:
+        offs[name] = (o, t.numel() * t.element_size())
+        o = align(o + t.numel() * t.element_size())
+    in_bytes = o
+
+    def pack(tab):
+        hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        for name, t in parts:
+            src = tab if name == "tab" else t
+            off, n = offs[name]
+            hb[off:off + n] = src.detach().cpu().contiguous().view(-1).view(torch.uint8)
+        return hb
+
+    hins = [pack(t) for t in step.tables]
+    o_bytes = step.out.numel() * step.out.element_size()
+    l_off = align(o_bytes)
+    res_bytes = l_off + step.lse.numel() * step.lse.element_size()
+    dbufs = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dress = [torch.empty(res_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    hress = [torch.empty(res_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    s_cmp, s_up, s_dn = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def dview(buf, name, like):
+        off, n = offs[name]
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    calls = []
+    for j in range(2):
+        dout = dress[j][:o_bytes].view(step.out.dtype).view(step.out.shape)
+        dlse = dress[j][l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
+        calls.append(va.prepare_paged(dview(dbufs[j], "q", step.q), step.pool,
+                                      dview(dbufs[j], "tab", step.tables[0]),
+                                      dview(dbufs[j], "ind", step.indptr),
+                                      dview(dbufs[j], "pre", step.prefix),
+                                      dview(dbufs[j], "par", step.parents),
+                                      sm_scale=synth.SM_SCALE, nsplit=step.nsplit,
+                                      flags=step.path, workspace=step.ws, out=dout, lse=dlse,
+                                      stream=s_cmp))
+
+    def run_steps(k0: int, n: int, origin):
+        """Enqueue steps k0 .. k0+n-1; `origin` is the stream the work forks
+        from and joins back to (the capturing stream inside a capture)."""
+        ev_in = [None, None]     # buffer j's inputs consumed (its last call done)
+        ev_out = [None, None]    # result buffer j read back
+        start = torch.cuda.Event()
+        start.record(origin)
+        for s_ in (s_cmp, s_up, s_dn):
+            s_.wait_event(start)
+        for k in range(k0, k0 + n):
+            j = k % 2
+            up = torch.cuda.Event()
+            with torch.cuda.stream(s_up):
+                if ev_in[j] is not None:
+                    s_up.wait_event(ev_in[j])
+                dbufs[j].copy_(hins[k % len(hins)], non_blocking=True)
+                up.record(s_up)
+            s_cmp.wait_event(up)
+            if ev_out[j] is not None:
+                s_cmp.wait_event(ev_out[j])
+            calls[j]()
+            done = torch.cuda.Event()
+            done.record(s_cmp)
+            ev_in[j] = done
+            with torch.cuda.stream(s_dn):
+                s_dn.wait_event(done)
+                hress[j].copy_(dress[j], non_blocking=True)
+                dn = torch.cuda.Event()
+                dn.record(s_dn)
+            ev_out[j] = dn
+        for s_ in (s_cmp, s_up, s_dn):
+            e = torch.cuda.Event()
+            e.record(s_)
+            origin.wait_event(e)
+
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    # eager warm-up, and a check that the copy path computes the same step
+    run_steps(0, 2, cap)
+    torch.cuda.synchronize()
+    ref0 = dress[0].clone()
+    step.call(0)
+    torch.cuda.synchronize()
+    dout0 = ref0[:o_bytes].view(step.out.dtype).view(step.out.shape)
+    dlse0 = ref0[l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
+    assert torch.equal(dout0, step.out) and torch.equal(dlse0, step.lse), "e2e path differs"
+    assert torch.equal(hress[0], ref0.cpu()), "e2e read-back differs"
+    per = STEPS_PER_GRAPH
+    graphs = []
+    for gi in range(max(1, min(4, len(hins) // per))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            run_steps(gi * per, per, cap)
+        graphs.append(g)
+    tail = None
+    if K % per:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=cap):
+            run_steps(0, K % per, cap)
+    with torch.cuda.stream(cap):
+        for r in range(max(1, -(-W // per))):
+            graphs[r % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cap):
+        a.record()
+        for r in range(K // per):
+            graphs[r % len(graphs)].replay()
+        if tail is not None:
+            tail.replay()
+        b.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e_ms = max_over_ranks(a.elapsed_time(b) / K, dist, dev)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": job_gbs(world, step.kv_bytes, 1, e_ms), "unit": "GB/s",
+            "us_per_step": e_ms * 1e3, "steps": K, "h2d_bytes_per_step": int(in_bytes),
+            "d2h_bytes_per_step": int(res_bytes),
+            "note": "every step: its inputs packed in one pinned buffer and copied in (one H2D "
+                    "copy), the verify call (prepared once with va.prepare_paged) launched, out "
+                    "and lse read back (one D2H copy); two buffer sets alternate so that the "
+                    "copies of neighbouring steps overlap a step's kernels on separate streams; "
+                    "steps captured eight to a CUDA graph and replayed"}
+
+
 # ------------------------------------------------------------------ main
+
+def bench_accept(va, dev, hbm_peak) -> dict:
+    """Greedy tree acceptance after verify: B=8 requests, T=16 nodes, a
+    129280-token vocabulary, fp32 logits (one row after the prefix and one per
+    node); rotated logits buffers larger than L2 together, CUDA graphs of 8
+    calls."""
+    ga = torch.Generator().manual_seed(9)
+    Ba, Ta, Va = 8, 16, 129280
+    nbuf = max(2, math.ceil(3 * torch.cuda.get_device_properties(dev).L2_cache_size
+                            / (Ba * (Ta + 1) * Va * 4)))
+    bufs = [(torch.randn(Ba, Va, generator=ga).to(dev), torch.randn(Ba, Ta, Va, generator=ga).to(dev))
+            for _ in range(nbuf)]
+    par_a = torch.stack([synth.make_parents(Ta, "random", ga) for _ in range(Ba)]).to(dev)
+    tok_a = torch.randint(0, Va, (Ba, Ta), generator=ga, dtype=torch.int32).to(dev)
+    slot_a = torch.arange(Ba * Ta, dtype=torch.int32, device=dev).reshape(Ba, Ta)
+    res = va.tree_accept(bufs[0][0], bufs[0][1], tok_a, par_a, slot_a)
+    ws_a, outs_a = res[4], res[:4]
+    sa = torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    ga_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga_graph, stream=sa):
+        for k in range(8):
+            va.tree_accept(bufs[k % nbuf][0], bufs[k % nbuf][1], tok_a, par_a, slot_a,
+                           workspace=ws_a, outputs=outs_a, stream=sa)
+    for _ in range(3):
+        ga_graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        ga_graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    a_us = e0.elapsed_time(e1) / (8 * reps) * 1e3
+    a_bytes = Ba * (Ta + 1) * Va * 4
+    del bufs
+    torch.cuda.empty_cache()
+    return {"us": a_us, "logits_bytes": a_bytes, "gbs": a_bytes / (a_us * 1e-6) / 1e9,
+            "frac_hbm": a_bytes / (a_us * 1e-6) / 1e9 / hbm_peak,
+            "timing": "CUDA graphs of 8 calls on rotated logits buffers (> L2 together), events"}
+
+
+def bench_defrag(va, pool, dev, hbm_peak) -> dict:
+    """65536 scattered rows (lower half of the pool) compacted into a
+    contiguous range in the upper half."""
+    gd = torch.Generator().manual_seed(7)
+    n = 65536
+    src = torch.randperm(pool.shape[0] // 2, generator=gd)[:n].to(torch.int32).to(dev)
+    sind = torch.tensor([0, n], dtype=torch.int32, device=dev)
+    dstb = torch.tensor([pool.shape[0] // 2], dtype=torch.int64, device=dev)
+    for _ in range(3):
+        va.verify_attn_defrag(pool, src, sind, dstb)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for _ in range(reps):
+        va.verify_attn_defrag(pool, src, sind, dstb)
+    e1.record()
+    torch.cuda.synchronize()
+    d_us = e0.elapsed_time(e1) / reps * 1e3
+    moved = 2 * n * synth.D_QK * 2
+    return {"us": d_us, "bytes_moved": moved, "gbs": moved / (d_us * 1e-6) / 1e9,
+            "frac_hbm": moved / (d_us * 1e-6) / 1e9 / hbm_peak}
+
 
 def main():
     args = parse()
@@ -519,176 +843,79 @@ def main():
     hbm_peak, tc_peak, peak_kind = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    # ---- headline workload
-    H, T, P = 8, 16, 4096
-    pool = device_pool(1 << 20, seed=1 + rank, dev=dev)
-    kv_step = (P + T) * synth.D_QK * 2
-    nrot = max(2, math.ceil(3 * l2 / kv_step))
-    step = Step(va, pool, H, T, P, seed=1 + rank, nrot=nrot, dev=dev, path=args.path,
-                nsplit=args.nsplit)
-    parity = check_parity(step, 0)
-
+    # ---- headline: the batched ragged step (8 requests, H=64, T=16)
+    hs = synth.spec(HEADLINE)
+    pool = device_pool(hs.num_slots, seed=1 + rank, dev=dev)
+    step = Step(va, pool, hs.H, hs.T, list(hs.prefix), seed=4 + rank, nrot=2, dev=dev,
+                path=args.path, nsplit=args.nsplit)
+    kv_step = step.kv_bytes
+    assert step.nrot * kv_step > 2 * l2, "rotated slot tables must exceed L2"
+    graphs, _ = capture_graphs(step, args.steps)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     t_wall0 = time.time()
-    ms, k_ms = measure(step, args.steps, args.warmup, dist)
+    ms = time_steps(graphs, args.steps, args.warmup, dist)
     t_wall1 = time.time()
     time.sleep(0.25)
     clocks.stop()
+    del graphs
     ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
     value = job_gbs(world, kv_step, args.steps, ms)
+    k_us = partial_kernel_us(step)
+    head = point_record(step, ms_step * 1e3, ms_step * 1e3, ms_step * 1e3, k_us, hbm_peak,
+                        tc_peak)
 
-    # ---- end to end through the public API with host buffers.  A step's
-    # inputs (q, its slot table, indptr, prefix lengths, parents) are packed
-    # in one pinned host buffer and land with one host-to-device copy in a
-    # device buffer whose views the call takes; out and lse are views of one
-    # device result buffer read back with one device-to-host copy.
-    def align(n):
-        return (n + 255) // 256 * 256
+    e2e = e2e_leg(va, step, args.steps, args.warmup, dist, dev)
 
-    parts = [("q", step.q), ("tab", step.tables[0]), ("par", step.parents),
-             ("ind", step.indptr), ("pre", step.prefix)]
-    offs, o = {}, 0
-    for name, t in parts:
-        offs[name] = (o, t.numel() * t.element_size())
-        o = align(o + t.numel() * t.element_size())
-    in_bytes = o
-
-    def pack(tab):
-        hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-        for name, t in parts:
-            src = tab if name == "tab" else t
-            off, n = offs[name]
-            hb[off:off + n] = src.detach().cpu().contiguous().view(-1).view(torch.uint8)
-        return hb
-
-    hins = [pack(t) for t in step.tables]
-    o_bytes = step.out.numel() * step.out.element_size()
-    l_off = align(o_bytes)
-    res_bytes = l_off + step.lse.numel() * step.lse.element_size()
-    h2d = in_bytes
-    d2h = res_bytes
-    Ke = min(args.steps, 500)
-
-    dbuf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-
-    def dview(name, like):
-        off, n = offs[name]
-        return dbuf[off:off + n].view(like.dtype).view(like.shape)
-
-    dres = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
-    dout = dres[:o_bytes].view(step.out.dtype).view(step.out.shape)
-    dlse = dres[l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
-    hres = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
-    # The verify call prepared once (checks and marshalling) on stream s; each
-    # step copies its packed inputs in, launches it and reads out and lse back.
-    # Steps are captured eight to a CUDA graph (the copies are graph nodes, each
-    # step's from its own pinned buffer), as a serving loop would replay them,
-    # so that Python does not pace the device.
-    s_e2e = torch.cuda.Stream()
-    s_e2e.wait_stream(torch.cuda.current_stream())
-    call = va.prepare_paged(dview("q", step.q), step.pool, dview("tab", step.tables[0]),
-                            dview("ind", step.indptr), dview("pre", step.prefix),
-                            dview("par", step.parents), sm_scale=synth.SM_SCALE,
-                            nsplit=step.nsplit, flags=step.path, workspace=step.ws, out=dout,
-                            lse=dlse, stream=s_e2e)
-
-    def e2e_step(k):
-        dbuf.copy_(hins[k % len(hins)], non_blocking=True)
-        call()
-        hres.copy_(dres, non_blocking=True)
-
-    with torch.cuda.stream(s_e2e):
-        for k in range(min(args.warmup, 20)):
-            e2e_step(k)
-        # the packed copy path computes the same step: check one result
-        e2e_step(0)
-    torch.cuda.synchronize()
-    step.call(0)
-    torch.cuda.synchronize()
-    assert torch.equal(dout, step.out) and torch.equal(dlse, step.lse), "e2e path differs"
-    assert torch.equal(hres, dres.cpu()), "e2e read-back differs"
-    per = STEPS_PER_GRAPH
-    e_graphs = []
-    for gi in range(max(1, min(8, len(hins) // per))):
-        g_e = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_e, stream=s_e2e):
-            for j2 in range(per):
-                e2e_step(gi * per + j2)
-        e_graphs.append(g_e)
-    Ke = (Ke // per) * per
-    with torch.cuda.stream(s_e2e):
-        for g_e in e_graphs:
-            g_e.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s_e2e):
-        a.record()
-        for r in range(Ke // per):
-            e_graphs[r % len(e_graphs)].replay()
-        b.record()
-    torch.cuda.synchronize()
-    e_ms = max_over_ranks(a.elapsed_time(b) / Ke, dist, dev)
-    e2e = {"value": job_gbs(world, kv_step, 1, e_ms), "unit": "GB/s",
-           "us_per_step": e_ms * 1e3, "steps": Ke, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h),
-           "note": "every step: its inputs packed in one pinned buffer and copied in "
-                   "(one H2D copy), the verify call (prepared once with va.prepare_paged) "
-                   "launched, out and lse read back (one D2H copy); steps captured eight "
-                   "to a CUDA graph and replayed"}
-
-    # ---- prefix sweeps (H=8 and H=64, T=16), scattered slots
-    sweep = []
+    # ---- the target points: H=8 and H=64, T=16, prefixes 16k / 65k / 200k,
+    # scattered and contiguous (kernel-level fractions of both roofs), and the
+    # rest of the prefix sweep
+    targets, sweep = [], []
     if not args.no_sweep and rank == 0:
-        points = [(Hs, Ps, "scattered") for Hs in (8, 64) for Ps in SWEEP_P]
-        points += [(Hs, Ps, "contiguous") for Hs in (8, 64) for Ps in (16384, 65536, 200000)]
-        for Hs, Ps, lay in points:
-            if True:
-                kvb = (Ps + 16) * synth.D_QK * 2
-                nr = max(1, min(16, math.ceil(3 * l2 / kvb)))
-                st = Step(va, pool, Hs, 16, Ps, seed=7, nrot=nr, dev=dev, path=args.path,
-                          nsplit=0, layout=lay)
-                reps = 8 * math.ceil(max(20, min(400, int(2e5 / (Ps / 1024 * Hs / 8)))) / 8)
-                us, p10, p90, k_us = measure_dist(st, reps, 5)
-                sweep.append({"H": Hs, "T": 16, "P": Ps, "layout": lay, "us_per_step": us,
-                              "p10": p10, "p90": p90,
-                              "gbs": kvb / (us * 1e-6) / 1e9,
-                              "frac_hbm": kvb / (us * 1e-6) / 1e9 / hbm_peak,
-                              "tflops": st.flops / (us * 1e-6) / 1e12,
-                              "partial_kernel_us": k_us,
-                              "partial_gbs": kvb / (k_us * 1e-6) / 1e9, "nsplit": st.nsplit,
-                              "path": "auto" if args.path == 0 else str(args.path)})
-                del st
-                torch.cuda.empty_cache()
+        points = [(H_, P_, lay, True) for H_ in (8, 64) for P_ in TARGET_P
+                  for lay in ("scattered", "contiguous")]
+        points += [(H_, P_, "scattered", False) for H_ in (8, 64) for P_ in SWEEP_P]
+        for H_, P_, lay, is_target in points:
+            kvb = (P_ + 16) * synth.D_QK * 2
+            nr = max(1, min(16, math.ceil(3 * l2 / kvb)))
+            st = Step(va, pool, H_, 16, P_, seed=7, nrot=nr, dev=dev, path=args.path,
+                      nsplit=0, layout=lay)
+            reps = 8 * math.ceil(max(16, min(400, int(2e5 / (P_ / 1024 * H_ / 8)))) / 8)
+            us, p10, p90, k_us_ = measure_dist(st, reps, 5)
+            rec = {"H": H_, "T": 16, "P": P_, "layout": lay}
+            rec.update(point_record(st, us, p10, p90, k_us_, hbm_peak, tc_peak))
+            rec["bound"] = "hbm" if 2176 * 16 * H_ / 1152 < tc_peak * 1e12 / (hbm_peak * 1e9) \
+                else "tensor"
+            (targets if is_target else sweep).append(rec)
+            del st
+            torch.cuda.empty_cache()
 
-    # ---- the remaining configurations of the step, and the defrag compaction
+    # ---- the other configurations of the step, and the widened rows
     configs = {}
     if not args.no_sweep and rank == 0:
+        # TP8 slice: H=8, T=16, prefix 4096 (launch-bound)
+        st = Step(va, pool, 8, 16, 4096, seed=1, nrot=max(2, math.ceil(3 * l2 / (4112 * 1152))),
+                  dev=dev, path=args.path, nsplit=0)
+        med, p10, p90, k_us_ = measure_dist(st, 64, 8)
+        configs["tp8 slice H=8 T=16 P=4096 scattered"] = point_record(
+            st, med, p10, p90, k_us_, hbm_peak, tc_peak)
+        del st
         # long context: H=8, T=32 random tree, prefix 200000, 2^18-slot pool,
         # nsplit swept (two 128-row blocks per split)
         pool_l = device_pool(1 << 18, seed=3, dev=dev)
         rows = []
         for ns in (16, 32, 64, 96, 128, 0):
-            st = Step(va, pool_l, 8, 32, 200000, seed=3, nrot=1, dev=dev, path=args.path, nsplit=ns)
-            med, p10, p90, k_us = measure_dist(st, 16, 3)
-            rows.append({"nsplit": st.nsplit, "auto": ns == 0, "us_per_step": med, "p10": p10,
-                         "p90": p90, "gbs": st.kv_bytes / (med * 1e-6) / 1e9,
-                         "tflops": st.flops / (med * 1e-6) / 1e12, "partial_kernel_us": k_us})
+            st = Step(va, pool_l, 8, 32, 200000, seed=3, nrot=1, dev=dev, path=args.path,
+                      nsplit=ns)
+            med, p10, p90, k_us_ = measure_dist(st, 16, 3)
+            r = {"auto": ns == 0}
+            r.update(point_record(st, med, p10, p90, k_us_, hbm_peak, tc_peak))
+            rows.append(r)
             del st
-        configs["long H=8 T=32 P=200000 scattered (2^18 pool)"] = rows
+        configs["long H=8 T=32 P=200000 scattered (2^18 pool), nsplit sweep"] = rows
         del pool_l
-        torch.cuda.empty_cache()
-        # batched ragged: 8 requests, prefixes U[1024, 65536], H=64, T=16
-        prefs = synth.spec("batched").prefix
-        st = Step(va, pool, 64, 16, prefs, seed=4, nrot=2, dev=dev, path=args.path, nsplit=0)
-        med, p10, p90, k_us = measure_dist(st, 8, 3)
-        configs["batched B=8 H=64 T=16 ragged, one graph per step"] = {
-            "prefixes": prefs, "nsplit": st.nsplit, "us_per_step": med, "p10": p10, "p90": p90,
-            "gbs": st.kv_bytes / (med * 1e-6) / 1e9, "tflops": st.flops / (med * 1e-6) / 1e12,
-            "partial_kernel_us": k_us, "kv_bytes": st.kv_bytes}
-        del st
         torch.cuda.empty_cache()
         # segmented call (two slot lists + dense extend mask) on the TP8 slice,
         # beside the paged call on the same slots
@@ -696,101 +923,49 @@ def main():
         for lay in ("segmented", "segmented_append", "scattered"):
             st = Step(va, pool, 8, 16, 4096, seed=1, nrot=16, dev=dev, path=args.path, nsplit=0,
                       layout=lay)
-            med, p10, p90, k_us = measure_dist(st, 64, 8)
+            med, p10, p90, k_us_ = measure_dist(st, 64, 8)
             seg[lay] = {"us_per_step": med, "p10": p10, "p90": p90,
-                        "gbs": st.kv_bytes / (med * 1e-6) / 1e9, "partial_kernel_us": k_us}
+                        "gbs": st.kv_bytes / (med * 1e-6) / 1e9, "kernel_us": k_us_}
             del st
         configs["segmented TP8 H=8 T=16 P=4096 (kv_indices + out_cache_loc + dense mask; "
                 "with the draft rows appended in the call) vs paged"] = seg
         torch.cuda.empty_cache()
-        # greedy tree acceptance after verify: B=8 requests, T=16 nodes, a
-        # 129280-token vocabulary, fp32 logits (one row after the prefix and
-        # one per node); rotated logits buffers larger than L2 together
-        ga = torch.Generator().manual_seed(9)
-        Ba, Ta, Va = 8, 16, 129280
-        nbuf = max(2, math.ceil(3 * torch.cuda.get_device_properties(dev).L2_cache_size
-                                / (Ba * (Ta + 1) * Va * 4)))
-        bufs = [(torch.randn(Ba, Va, generator=ga).to(dev), torch.randn(Ba, Ta, Va, generator=ga).to(dev))
-                for _ in range(nbuf)]
-        par_a = torch.stack([synth.make_parents(Ta, "random", ga) for _ in range(Ba)]).to(dev)
-        tok_a = torch.randint(0, Va, (Ba, Ta), generator=ga, dtype=torch.int32).to(dev)
-        slot_a = torch.arange(Ba * Ta, dtype=torch.int32, device=dev).reshape(Ba, Ta)
-        res = va.tree_accept(bufs[0][0], bufs[0][1], tok_a, par_a, slot_a)
-        ws_a, outs_a = res[4], res[:4]
-        # graphs of 8 calls, each on its own logits buffer, as for the verify step
-        sa = torch.cuda.Stream()
-        sa.wait_stream(torch.cuda.current_stream())
-        ga_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga_graph, stream=sa):
-            for k in range(8):
-                va.tree_accept(bufs[k % nbuf][0], bufs[k % nbuf][1], tok_a, par_a, slot_a,
-                               workspace=ws_a, outputs=outs_a, stream=sa)
-        for _ in range(3):
-            ga_graph.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 10
-        e0.record()
-        for _ in range(reps):
-            ga_graph.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        a_us = e0.elapsed_time(e1) / (8 * reps) * 1e3
-        a_bytes = Ba * (Ta + 1) * Va * 4
-        configs["tree acceptance B=8 T=16 V=129280 fp32 logits"] = {
-            "us": a_us, "logits_bytes": a_bytes, "gbs": a_bytes / (a_us * 1e-6) / 1e9,
-            "frac_hbm": a_bytes / (a_us * 1e-6) / 1e9 / hbm_peak,
-            "timing": "CUDA graphs of 8 calls on rotated logits buffers (> L2 together), events"}
-        del bufs
-        torch.cuda.empty_cache()
-        # defrag: 65536 scattered rows (lower half of the pool) compacted into a
-        # contiguous range in the upper half
-        gd = torch.Generator().manual_seed(7)
-        n = 65536
-        src = torch.randperm(pool.shape[0] // 2, generator=gd)[:n].to(torch.int32).to(dev)
-        sind = torch.tensor([0, n], dtype=torch.int32, device=dev)
-        dstb = torch.tensor([pool.shape[0] // 2], dtype=torch.int64, device=dev)
-        for _ in range(3):
-            va.verify_attn_defrag(pool, src, sind, dstb)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 20
-        e0.record()
-        for _ in range(reps):
-            va.verify_attn_defrag(pool, src, sind, dstb)
-        e1.record()
-        torch.cuda.synchronize()
-        d_us = e0.elapsed_time(e1) / reps * 1e3
-        moved = 2 * n * synth.D_QK * 2
-        configs["defrag 65536 scattered rows -> contiguous"] = {
-            "us": d_us, "bytes_moved": moved, "gbs": moved / (d_us * 1e-6) / 1e9,
-            "frac_hbm": moved / (d_us * 1e-6) / 1e9 / hbm_peak}
+        configs["tree acceptance B=8 T=16 V=129280 fp32 logits"] = bench_accept(va, dev,
+                                                                                   hbm_peak)
+        configs["defrag 65536 scattered rows -> contiguous"] = bench_defrag(va, pool, dev,
+                                                                            hbm_peak)
 
-    cpu = None
+    cpu, parity = (None, None)
     if rank == 0 and not args.no_cpu:
-        cpu = cpu_oracle(P, H, T, seed=1)
+        cpu, parity = cpu_baseline_leg(step)
 
     clk = clocks.summary(t_wall0, t_wall1) or clocks.summary()
-    achieved = kv_step / (k_ms * 1e-3) / 1e9
+    achieved = step.flops / (k_us * 1e-6) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q and KV, random trees, random slot scatter)",
-        "config": {"workload": WORKLOAD, "B": 1, "H": H, "T": T, "prefix": P,
-                   "kv_bytes_per_step": kv_step, "nsplit": step.nsplit,
-                   "path": ["auto", "fma", "tc"][args.path],
-                   "l2": f"inputs larger than L2: {step.nrot} rotating slot tables "
-                         f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
-                   "launch": f"CUDA graphs of {STEPS_PER_GRAPH} steps, programmatic dependent "
-                             "launch between the kernels of a step",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": recorded_traffic(),
-                     "kernel": "split-K partial", "kernel_us": k_ms * 1e3,
-                     "peak_source": f"{peak_kind} hbm_gbs"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (3 if args.path == 1 else 2) * args.steps, "clocks": clk,
-        "parity": parity, "sweep": sweep, "configs": configs,
+        "config": dict(headline_config(),
+                       nsplit=step.nsplit, path=["auto", "fma", "tc"][args.path],
+                       l2=f"inputs larger than L2: {step.nrot} rotating slot tables "
+                          f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
+                       launch=f"CUDA graphs of {STEPS_PER_GRAPH} steps (plus one graph of the "
+                              f"{args.steps % STEPS_PER_GRAPH} remaining steps when --steps is "
+                              "not a multiple of 8): exactly --steps steps timed; programmatic "
+                              "dependent launch between the kernels of a step",
+                       parallelism=f"replicas x{world}"),
+        "headline": head,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": recorded_traffic(),
+                     "kernel": "split-K partial (partial_tc_kernel)", "kernel_us": k_us,
+                     "flops_per_launch": step.flops,
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                     "hbm_frac_of_kernel": kv_step / (k_us * 1e-6) / 1e9 / hbm_peak},
+        "target_points": targets,
+        "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
+        "gpu_launches": (3 if args.path == 1 else 2) * args.steps, "clocks": clk,
+        "sweep": sweep, "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

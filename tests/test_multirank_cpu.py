@@ -77,3 +77,7 @@ def test_reference_arm_under_two_ranks_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload description as the native arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == bench.headline_config()
