@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libverifyattn.so")
+# The test build: the same sources with VA_TEST_HOOKS, which adds the
+# producer gate declared in include/verify_attn_testhooks.h (used only by the
+# bounded-wait test; the product library never contains it).
+TESTHOOKS_LIB = os.path.join(OUT_DIR, "libverifyattn_testhooks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,29 +38,36 @@ def sources():
 
 def _deps():
     files = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
-    files.append(os.path.join(INCLUDE, "verify_attn.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          testhooks: bool = False) -> str:
+    """Builds libverifyattn.so, or with testhooks=True the test build
+    libverifyattn_testhooks.so; returns the library's path."""
+    lib = TESTHOOKS_LIB if testhooks else LIB
+    if not force and up_to_date(lib):
+        return lib
+    obj_dir = os.path.join(OUT_DIR, "testhooks") if testhooks else OUT_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-I", INCLUDE, "-I", CSRC,
                      "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
+    if testhooks:
+        common += ["-DVA_TEST_HOOKS"]
     if ptxas_v:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,15 +78,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                ptxas_v="--ptxas" in sys.argv))
+                ptxas_v="--ptxas" in sys.argv, testhooks="--testhooks" in sys.argv))

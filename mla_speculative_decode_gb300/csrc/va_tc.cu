@@ -52,6 +52,20 @@ extern "C" __attribute__((visibility("default"))) int va_trace_set(void* buf) {
 }
 #endif
 
+#ifdef VA_TEST_HOOKS
+// Test build only (libverifyattn_testhooks.so): a gate that the producer
+// warps of every split-K CTA wait on, bounded like every other wait, before
+// their first copy.  A test points it at a device flag that nothing sets, so
+// the wait runs out, and checks that the kernel gives up cleanly: status
+// VA_STATUS_TIMEOUT, every role leaves through its abort path, and the next
+// call on the stream is correct.  NULL (the default) = no gate.
+__device__ const int32_t* g_va_test_gate = nullptr;
+extern "C" __attribute__((visibility("default"))) int va_test_set_gate(const int32_t* flag) {
+  return cudaMemcpyToSymbol(g_va_test_gate, &flag, sizeof(flag)) == cudaSuccess ? VA_OK
+                                                                               : VA_ERR_CUDA;
+}
+#endif
+
 namespace va {
 namespace {
 
@@ -211,6 +225,18 @@ __device__ __forceinline__ int checked_row(const Params& p, int raw) {
 // boxes are used).  Returns false when a bounded wait gave up (all producers
 // agree through the named barrier).  Keys without a valid pool row set
 // VA_STATUS_BAD_SLOT in the CTA's status word `cta_flags` (shared memory).
+#ifdef VA_TEST_HOOKS
+// Bounded wait for a device flag to become non-zero (test gate).
+__device__ __noinline__ bool gate_wait(const int32_t* flag, long long limit_cycles) {
+  const long long t0 = clock64();
+  while (*reinterpret_cast<const volatile int32_t*>(flag) == 0) {
+    if (clock64() - t0 > limit_cycles) return false;
+    __nanosleep(2000);
+  }
+  return true;
+}
+#endif
+
 template <int kBlocks, int kRing, bool kMask>
 __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, const SplitRange& sr,
                                         int ntiles, int ptid, uint32_t ring, uint32_t full0,
@@ -223,6 +249,16 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   const int lane = ptid & 31;
   bool ok = true;
   bool bad_slot = false;
+#ifdef VA_TEST_HOOKS
+  {
+    bool open = true;
+    if (ptid == 0 && g_va_test_gate) open = gate_wait(g_va_test_gate, kWaitCycles);
+    if (!named_sync_and(kProducerBar, kProducers, open)) return false;
+  }
+#endif
+  // the last two tiles whose boxes producer 0 issued (-1: none), drained
+  // below if a wait gives up while they are in flight
+  int box_tile[2] = {-1, -1};
   VA_PH_DECL;
   for (int t = 0; t < ntiles; ++t) {
     const int g0 = kBlocks * t;   // ring position of the tile's first block
@@ -282,6 +318,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     if (kMask && ptid == 0) mbar_arrive(vready0 + 8u * uint32_t(t % kValidRing));
     if (ptid == 0) {
       if (boxes) {
+        box_tile[t & 1] = t;
         mbar_arrive_expect_tx(fb, uint32_t(kBlocks) * kBlockBytes);
         if (box3d && s0 + kBlocks <= kRing) {
           tma_load_3d(ring + uint32_t(s0) * kBlockBytes, map3, 0, int(row0), 0, fb);
@@ -327,6 +364,16 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
   }
   if (ptid == 0) VA_PH_STORE(kMask ? 11 : 12);
   cp_async_wait_all();
+  // After a wait gave up, the boxes still in flight land before the CTA can
+  // leave.  Only the last two tiles can be: a tile's slots are refilled only
+  // after the products of the tile two back have read them, so that tile's
+  // data had landed.  Every issued tile received all of its arrivals, and no
+  // later phase of its barrier can complete, so the parity wait is exact.
+  if (!ok && ptid == 0)
+    for (int i = 0; i < 2; ++i)
+      if (box_tile[i] >= 0)
+        (void)mbar_wait(full0 + 8u * uint32_t(box_tile[i] & 1), uint32_t(box_tile[i] >> 1) & 1u,
+                        nullptr, kWaitCycles);
   if (kMask && bad_slot) atomicOr(cta_flags, VA_STATUS_BAD_SLOT);
   return ok;
 }
@@ -508,6 +555,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) VA_PH_STORE(9);
       mma_commit_warp(bar(B_MMAFIN));
       mbar_wait(bar(B_MMAFIN), 0, nullptr, kWaitCycles);
+      // the Q boxes this lane issued have landed before the CTA can leave
+      // (normally long since; after an abort, possibly not)
+      if (lane == 0) (void)mbar_wait(bar(B_QTMA), 0, nullptr, kWaitCycles);
       __syncwarp();
     } else if (warp >= 4) {
       // ---- softmax: warpgroup `half` owns columns [32*half, 32*half + 32) of

@@ -194,3 +194,25 @@ def test_tree_accept_workspace_and_errors(lib):
     assert f(*bad) == -3
     bad = list(base); bad[9] = 16
     assert f(*bad) == -4
+
+
+def test_test_build_exports_its_gate_and_the_product_does_not():
+    """libverifyattn_testhooks.so (VA_TEST_HOOKS) exports the product ABI plus
+    the declarations of include/verify_attn_testhooks.h; the product library
+    exports none of the test hooks."""
+    import subprocess
+    from mla_speculative_decode_gb300 import _builder
+    th_path = _builder.build(testhooks=True)
+    text = open(os.path.join(ROOT, "include", "verify_attn_testhooks.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    hooks = set(re.findall(r"^\s*(?:int|size_t)\s+(\w+)\s*\(", text, flags=re.M))
+    assert hooks == {"va_test_set_gate"}
+
+    def exported(path):
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                             text=True, check=True).stdout
+        return {l.split()[-1] for l in out.splitlines() if " T " in l}
+
+    th = {s for s in exported(th_path) if s.startswith(("va_", "verify_attn"))}
+    assert th == set(declared_functions()) | hooks
+    assert not (exported(va.LIB_PATH) & hooks)
