@@ -27,6 +27,16 @@ Functions and the passages they follow (page titles and sections):
                    Checkpoint Report, "Input Knowledge Required to Understand
                    This Message" (a drafter proposes a tree of candidate tokens,
                    the target model checks them in one parallel pass).
+  tree_build, pop_slots
+                -- The Checkpoint Report, "Input Knowledge Required to
+                   Understand This Message" (a drafter proposes candidate
+                   tokens; DDTree builds a tree of draft tokens from them) and
+                   The Commit That Locked In 6x Decode, "4. The Marshaling
+                   Realization" (the per-step tree build, done on the host);
+                   the draft tokens' slots are out_cache_loc (The Checkpoint
+                   Report, "Mistakes and Incorrect Assumptions").  The pages
+                   give no selection rule: this is the best-first reading
+                   (highest cumulative log-probability first).
   segmented_lists, dense_mask_bits, append_rows
                 -- The Checkpoint Report, "Mistakes and Incorrect Assumptions"
                    (the extend call takes the prefix slots in kv_indices, the
@@ -293,6 +303,83 @@ def tree_accept(root_logits, logits, tokens, parent, slots=None):
             cur, t = c, target_token(lg[b, c])
         alen[b], bonus[b] = n, t
     return alen, nodes, aslots, bonus, bad
+
+
+def _valid_logp(x: np.float32) -> np.float32:
+    """A log-probability as the tree build reads it: NaN and +inf are not
+    log-probabilities and count as -inf."""
+    return np.float32(-np.inf) if (x != x or x == np.inf) else np.float32(x)
+
+
+def tree_build(cand_tokens, cand_logp, T: int):
+    """Draft tree of each request from the drafter's per-depth candidates.
+
+    cand_tokens int [B, D, K], cand_logp float32 [B, D, K]: at depth d (the
+    d+1-th draft position) the drafter proposes K tokens with their
+    log-probabilities.  A tree node is a path of candidate choices, one per
+    depth from depth 0 down; its score is the float32 running sum of the
+    chosen log-probabilities, root first.  The tree is grown best first:
+      1. at each depth, order the candidates by log-probability, highest
+         first, ties by lower candidate index (NaN and +inf count as -inf);
+      2. start from the empty tree; T times, add the highest-scoring node
+         whose parent is in the tree (depth-0 nodes hang off the prefix),
+         ties going to the shallower node, then to the path whose ranks are
+         lexicographically smaller.
+    Nodes are numbered in the order they were added, so a parent always
+    precedes its children.  Returns (parent int32 [B, T] (-1: hangs off the
+    prefix), tokens int32 [B, T], depth int32 [B, T] (0-based), ranks:
+    a list per request of each node's rank path).
+    """
+    import heapq
+    tok = np.asarray(cand_tokens)
+    lp = np.asarray(cand_logp, dtype=np.float32)
+    B, D, K = tok.shape
+    parent = np.zeros((B, T), dtype=np.int32)
+    tokens = np.zeros((B, T), dtype=np.int32)
+    depth = np.zeros((B, T), dtype=np.int32)
+    all_paths = []
+    for b in range(B):
+        # 1. candidates of each depth in order
+        order, slp = [], []
+        for d in range(D):
+            vals = [_valid_logp(lp[b, d, k]) for k in range(K)]
+            o = sorted(range(K), key=lambda k: (-float(vals[k]), k))
+            order.append(o)
+            slp.append([vals[k] for k in o])
+        # 2. best first.  Every node whose parent is in the tree is reachable
+        # as either the first child of a node in the tree or the next sibling
+        # (next rank) of a node in the tree, so a heap holding, for each node
+        # added, its first child and its next sibling always contains the best
+        # candidate.  Heap entries: (-score, depth, ranks, score, parent
+        # index, parent score), so the heap pops the order of step 2.
+        zero = np.float32(0)
+        heap = [(-float(slp[0][0]), 0, (0,), np.float32(zero + slp[0][0]), -1, zero)]
+        paths = []
+        for i in range(T):
+            _, d, ranks, sc, par, psc = heapq.heappop(heap)
+            parent[b, i] = par
+            tokens[b, i] = int(tok[b, d, order[d][ranks[-1]]])
+            depth[b, i] = d
+            paths.append(ranks)
+            if d + 1 < D:                       # first child
+                c = np.float32(sc + slp[d + 1][0])
+                heapq.heappush(heap, (-float(c), d + 1, ranks + (0,), c, i, sc))
+            if ranks[-1] + 1 < K:               # next sibling
+                c = np.float32(psc + slp[d][ranks[-1] + 1])
+                heapq.heappush(heap, (-float(c), d, ranks[:-1] + (ranks[-1] + 1,), c, par, psc))
+        all_paths.append(paths)
+    return parent, tokens, depth, all_paths
+
+
+def pop_slots(free_slots, head: int, B: int, T: int):
+    """Draft node i of request b takes free_slots[head + b*T + i]; returns
+    (out_cache_loc int32 [B*T] (-1 where the list has run out), new head)."""
+    fs = np.asarray(free_slots).reshape(-1)
+    loc = np.full(B * T, -1, dtype=np.int32)
+    for j in range(B * T):
+        if 0 <= head + j < fs.shape[0]:
+            loc[j] = fs[head + j]
+    return loc, head + B * T
 
 
 def defrag(pool_bits, src_slots, src_indptr, dst_base):

@@ -589,3 +589,129 @@ def test_defrag_copies_rows_and_preserves_attention(oracle_mod):
                                            w.prefix_len.numpy(), bits, w.spec.sm_scale)
     np.testing.assert_array_equal(out0, out1)
     np.testing.assert_array_equal(lse0, lse1)
+
+
+# ------------------------------------------------------- draft tree build
+
+def test_tree_build_golden(oracle_mod):
+    g = _parse(os.path.join(GOLDEN, "tree_build_small.txt"))
+    D = sum(1 for k in g if k.startswith("tokens") and k[6:].isdigit())
+    tok = np.array([[[int(x) for x in g[f"tokens{d}"].split()] for d in range(D)]])
+    lp = np.array([[[float(x) for x in g[f"logp{d}"].split()] for d in range(D)]],
+                  dtype=np.float32)
+    T = int(g["T"])
+    par, tk, dp, _ = oracle_mod.tree_build(tok, lp, T)
+    ints = lambda k: [int(x) for x in g[k].split()]
+    assert par[0].tolist() == ints("parent")
+    assert tk[0].tolist() == ints("tokens")
+    assert dp[0].tolist() == ints("depth")
+
+
+def _brute_paths(lp_sorted, D, K):
+    """Every node of the candidate tree (rank paths of length 1..D) with its
+    float32 running score, by exhaustive enumeration."""
+    import itertools
+    out = []
+    for d in range(1, D + 1):
+        for ranks in itertools.product(range(K), repeat=d):
+            s = np.float32(0)
+            for i, r in enumerate(ranks):
+                s = np.float32(s + lp_sorted[i][r])
+            out.append((ranks, s))
+    return out
+
+
+def _sorted_candidates(tok, lp):
+    """Per depth: candidates by log-probability (NaN/+inf -> -inf), highest first."""
+    D, K = tok.shape
+    ts, ls = [], []
+    for d in range(D):
+        v = [np.float32(-np.inf) if (x != x or x == np.inf) else np.float32(x) for x in lp[d]]
+        o = sorted(range(K), key=lambda k: (-float(v[k]), k))
+        ts.append([int(tok[d][k]) for k in o])
+        ls.append([v[k] for k in o])
+    return ts, ls
+
+
+def _as_tree(paths, ts):
+    """(parent, tokens, depth) of rank paths listed in tree order."""
+    idx = {p: i for i, p in enumerate(paths)}
+    parent = [idx[p[:-1]] if len(p) > 1 else -1 for p in paths]
+    return parent, [ts[len(p) - 1][p[-1]] for p in paths], [len(p) - 1 for p in paths]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tree_build_is_the_global_top_T_for_log_probabilities(oracle_mod, seed):
+    """With log-probabilities (all <= 0) a child never outscores its parent,
+    so growing the tree best first selects the T best nodes of the whole
+    candidate tree: here every node is enumerated and sorted (score desc,
+    depth asc, rank path asc) and the first T compared with the oracle."""
+    rng = np.random.default_rng(seed)
+    B, D, K = 3, 4, 3
+    tok = rng.integers(0, 50, size=(B, D, K))
+    lp = np.log(rng.dirichlet(np.ones(K), size=(B, D))).astype(np.float32)
+    if seed % 2:               # quantise to force ties
+        lp = (np.round(lp * 2) / 2).astype(np.float32)
+    if seed == 5:
+        lp[0, 1, 2] = np.nan
+        lp[1, 0, 0] = -np.inf
+    T = int(rng.integers(1, 30))
+    par, tk, dp, _ = oracle_mod.tree_build(tok, lp, T)
+    for b in range(B):
+        ts, ls = _sorted_candidates(tok[b], lp[b])
+        nodes = _brute_paths(ls, D, K)
+        nodes.sort(key=lambda n: (-float(n[1]), len(n[0]), n[0]))
+        want = _as_tree([n[0] for n in nodes[:T]], ts)
+        assert par[b].tolist() == want[0]
+        assert tk[b].tolist() == want[1]
+        assert dp[b].tolist() == want[2]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tree_build_equals_a_scan_of_every_attachable_node(oracle_mod, seed):
+    """Best first with no heap: at each step every node whose parent is already
+    in the tree is scored and the best taken (same tie rule).  Holds for any
+    scores, including positive ones (raw logits passed by mistake), where the
+    tree is no longer the global top T."""
+    rng = np.random.default_rng(100 + seed)
+    B, D, K = 2, 3, 4
+    tok = rng.integers(0, 9, size=(B, D, K))
+    lp = rng.normal(0, 1.5, size=(B, D, K)).astype(np.float32)
+    if seed % 2:
+        lp = np.round(lp).astype(np.float32)
+    T = int(rng.integers(1, 40))
+    par, tk, dp, _ = oracle_mod.tree_build(tok, lp, T)
+    for b in range(B):
+        ts, ls = _sorted_candidates(tok[b], lp[b])
+        score = {p: s for p, s in _brute_paths(ls, D, K)}
+        chosen = []
+        for _ in range(T):
+            have = set(chosen)
+            cand = [p for p in score if p not in have and (len(p) == 1 or p[:-1] in have)]
+            best = min(cand, key=lambda p: (-float(score[p]), len(p), p))
+            chosen.append(best)
+        want = _as_tree(chosen, ts)
+        assert par[b].tolist() == want[0]
+        assert tk[b].tolist() == want[1]
+        assert dp[b].tolist() == want[2]
+
+
+def test_tree_build_peaked_drafter_gives_a_chain(oracle_mod):
+    """A drafter certain of one token per depth (log-prob 0 there, -30 for the
+    others): the first D nodes are the chain of those tokens."""
+    D, K = 6, 4
+    tok = np.arange(D * K).reshape(1, D, K)
+    lp = np.full((1, D, K), -30.0, dtype=np.float32)
+    lp[0, np.arange(D), np.arange(D) % K] = 0.0
+    par, tk, dp, _ = oracle_mod.tree_build(tok, lp, D)
+    assert par[0].tolist() == [-1] + list(range(D - 1))
+    assert tk[0].tolist() == [d * K + d % K for d in range(D)]
+    assert dp[0].tolist() == list(range(D))
+
+
+def test_pop_slots(oracle_mod):
+    free = np.array([7, 3, 9, 1, 4, 8], dtype=np.int32)
+    loc, head = oracle_mod.pop_slots(free, 1, 2, 2)
+    assert loc.tolist() == [3, 9, 1, 4] and head == 5
+    loc, head = oracle_mod.pop_slots(free, 4, 2, 2)    # the list runs out
+    assert loc.tolist() == [4, 8, -1, -1] and head == 8
