@@ -795,6 +795,39 @@ def bench_accept(va, dev, hbm_peak) -> dict:
             "timing": "CUDA graphs of 8 calls on rotated logits buffers (> L2 together), events"}
 
 
+def bench_tree_build(va, dev) -> dict:
+    """Device-side draft tree and slot building: B=8 requests, D=8 draft
+    positions with K=8 candidates each, T=16 nodes; CUDA graphs of 8 calls
+    (the free-list head moves on with every call)."""
+    rng = np.random.default_rng(21)
+    B, D, K, T = 8, 8, 8, 16
+    tok = torch.from_numpy(rng.integers(0, 129280, size=(B, D, K)).astype(np.int32)).to(dev)
+    lp = torch.from_numpy(np.log(rng.dirichlet(np.ones(K), size=(B, D))).astype(np.float32)).to(dev)
+    free = torch.randperm(1 << 20, dtype=torch.int32, device=dev)
+    head = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = va.tree_build(tok, lp, T, free, head)
+    s_ = torch.cuda.Stream()
+    s_.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s_):
+        for _ in range(8):
+            va.tree_build(tok, lp, T, free, head, outputs=outs, stream=s_)
+    head.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return {"us": e0.elapsed_time(e1) / (8 * reps) * 1e3, "B": B, "D": D, "K": K, "T": T,
+            "timing": "CUDA graphs of 8 calls, events; the pages' host tree build took "
+                      "1.8 ms per step (sm_120 service, context only)"}
+
+
 def bench_defrag(va, pool, dev, hbm_peak) -> dict:
     """65536 scattered rows (lower half of the pool) compacted into a
     contiguous range in the upper half."""
@@ -932,6 +965,8 @@ def main():
         torch.cuda.empty_cache()
         configs["tree acceptance B=8 T=16 V=129280 fp32 logits"] = bench_accept(va, dev,
                                                                                    hbm_peak)
+        configs["tree build B=8 D=8 K=8 T=16 (draft tree + out_cache_loc on the device)"] = \
+            bench_tree_build(va, dev)
         configs["defrag 65536 scattered rows -> contiguous"] = bench_defrag(va, pool, dev,
                                                                             hbm_peak)
 

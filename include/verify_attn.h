@@ -258,6 +258,52 @@ int va_tree_accept(const float *root_logits, const float *logits, int64_t V,
                    int32_t *accept_slots, int32_t *bonus_token, va_stream_t stream);
 
 /*
+ * Draft tree and draft KV slots, built on the device from the drafter's
+ * output (The Checkpoint Report, "Input Knowledge Required to Understand
+ * This Message": a drafter proposes candidate tokens and DDTree builds a tree
+ * of draft tokens from them; The Commit That Locked In 6x Decode, "4. The
+ * Marshaling Realization": this per-step tree build ran on the host).  The
+ * pages give no selection rule; the drafter's output is read as K candidate
+ * tokens with log-probabilities at each of D draft positions, and the tree is
+ * grown best first:
+ *   - at each depth the candidates are ranked by log-probability, highest
+ *     first, ties by lower index (NaN and +inf count as -inf);
+ *   - a node is a path of one candidate per depth from depth 0 down; its
+ *     score is the float32 running sum of its log-probabilities, root first;
+ *   - T times, the highest-scoring node whose parent is already in the tree is
+ *     added (depth-0 nodes hang off the prefix); equal scores go to the
+ *     shallower node, then to the lexicographically smaller path of ranks.
+ * With log-probabilities (<= 0) this is the T best nodes of the whole
+ * candidate tree.  Node i of request b is the i-th node added, so parents
+ * precede children, as every verify call requires.
+ *   cand_tokens   int32 [B, D, K] device; cand_logp float [B, D, K] device.
+ *   1 <= D <= VA_TREE_MAX_DEPTH, 1 <= K <= VA_TREE_MAX_CAND,
+ *   1 <= T <= VA_T_MAX and T <= K + K^2 + ... + K^D.
+ *   tree_parent   int32 [B, T]: parent node, -1 for depth 0 (the layout
+ *                 every verify call and va_tree_accept take).
+ *   draft_tokens  int32 [B, T]: the candidate token of each node.
+ *   node_depth    int32 [B, T] or NULL: 0-based depth (the node's position
+ *                 after the prefix is prefix_len + depth).
+ *   free_slots    int32 [free_capacity] device, or NULL (no slots taken):
+ *                 pool slots available for new KV rows.  Node i of request b
+ *                 takes free_slots[*free_head + b*T + i] into
+ *                 out_cache_loc[b*T + i] (int32 [B*T]), -1 where the list has
+ *                 run out (and VA_STATUS_BAD_SLOT is set); then *free_head
+ *                 (int32, device) advances by B*T.  out_cache_loc is the list
+ *                 verify_attn_segmented takes.
+ *   status        uint32 device word or NULL: set to this call's status bits.
+ * One kernel launch, one CTA (a warp per request, eight at a time); no host
+ * sync, capture-safe: the free-list head is device state.  Returns VA_OK or a
+ * VA_ERR_* code.
+ */
+#define VA_TREE_MAX_DEPTH 15
+#define VA_TREE_MAX_CAND  16
+int va_tree_build(const int32_t *cand_tokens, const float *cand_logp, int B, int D, int K, int T,
+                  const int32_t *free_slots, int64_t free_capacity, int32_t *free_head,
+                  int32_t *tree_parent, int32_t *draft_tokens, int32_t *node_depth,
+                  int32_t *out_cache_loc, uint32_t *status, va_stream_t stream);
+
+/*
  * KV defragmentation (The Checkpoint Report, "Input Knowledge Required" and
  * "The Architecture of the Report": the deferred defragmentation phase).
  * For every request b and i < n_b = src_indptr[b+1] - src_indptr[b]:

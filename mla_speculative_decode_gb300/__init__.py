@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
     lib.va_tree_accept_workspace_bytes.restype = sz
     lib.va_tree_accept.argtypes = [P, P, i64, P, P, P, i32, i32, P, sz, P, P, P, P, P]
     lib.va_tree_accept.restype = i32
+    lib.va_tree_build.argtypes = [P, P, i32, i32, i32, i32, P, i64, P, P, P, P, P, P, P]
+    lib.va_tree_build.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
     lib.verify_attn_paged_noalloc.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32,
@@ -411,6 +413,65 @@ def tree_accept(root_logits: torch.Tensor, logits: torch.Tensor, draft_tokens: t
                                _ptr(bonus), _stream(stream))
     _check("va_tree_accept", rc)
     return alen, nodes, slots, bonus, workspace
+
+
+TREE_MAX_DEPTH = 15
+TREE_MAX_CAND = 16
+
+
+def tree_build(cand_tokens: torch.Tensor, cand_logp: torch.Tensor, T: int,
+               free_slots: Optional[torch.Tensor] = None,
+               free_head: Optional[torch.Tensor] = None, *, outputs=None,
+               status: Optional[torch.Tensor] = None, stream=None):
+    """Draft tree of each request from the drafter's candidates, on the device.
+
+    cand_tokens int32 [B, D, K], cand_logp fp32 [B, D, K]: K candidate tokens
+    with log-probabilities per draft position.  The tree is grown best first
+    (see va_tree_build in verify_attn.h).  With free_slots (int32) and
+    free_head (int32 [1], device), node i of request b takes the pool slot
+    free_slots[head + b*T + i] and the head advances by B*T.  Returns
+    (tree_parent int32 [B, T], draft_tokens int32 [B, T], node_depth int32
+    [B, T], out_cache_loc int32 [B*T] or None).  `outputs` = those tensors to
+    write into instead of new ones.
+    """
+    init(cand_logp.device.index)
+    _dev(cand_tokens, "cand_tokens", torch.int32)
+    _dev(cand_logp, "cand_logp", torch.float32)
+    if cand_tokens.dim() != 3 or tuple(cand_tokens.shape) != tuple(cand_logp.shape):
+        raise ValueError("cand_tokens and cand_logp must both be [B, D, K]")
+    B, D, K = cand_tokens.shape
+    dev = cand_logp.device
+    if (free_slots is None) != (free_head is None):
+        raise ValueError("free_slots and free_head go together")
+    if free_slots is not None:
+        _dev(free_slots, "free_slots", torch.int32)
+        _dev(free_head, "free_head", torch.int32)
+        if free_head.numel() != 1:
+            raise ValueError("free_head must hold one int32")
+    if outputs is None:
+        outputs = (torch.empty(B, T, dtype=torch.int32, device=dev),
+                   torch.empty(B, T, dtype=torch.int32, device=dev),
+                   torch.empty(B, T, dtype=torch.int32, device=dev),
+                   torch.empty(B * T, dtype=torch.int32, device=dev)
+                   if free_slots is not None else None)
+    par, tok, depth, loc = outputs
+    for t, n, size in ((par, "tree_parent", B * T), (tok, "draft_tokens", B * T),
+                       (depth, "node_depth", B * T), (loc, "out_cache_loc", B * T)):
+        if t is not None:
+            _dev(t, n, torch.int32)
+            if t.numel() != size:
+                raise ValueError(f"{n} must hold {size} entries")
+    if free_slots is not None and loc is None:
+        raise ValueError("out_cache_loc is needed with free_slots")
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    rc = load().va_tree_build(_ptr(cand_tokens), _ptr(cand_logp), B, D, K, int(T),
+                              _ptr(free_slots), 0 if free_slots is None else free_slots.numel(),
+                              _ptr(free_head), _ptr(par), _ptr(tok), _ptr(depth),
+                              _ptr(loc) if free_slots is not None else None, _ptr(status),
+                              _stream(stream))
+    _check("va_tree_build", rc)
+    return par, tok, depth, (loc if free_slots is not None else None)
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

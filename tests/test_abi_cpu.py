@@ -216,3 +216,28 @@ def test_test_build_exports_its_gate_and_the_product_does_not():
     th = {s for s in exported(th_path) if s.startswith(("va_", "verify_attn"))}
     assert th == set(declared_functions()) | hooks
     assert not (exported(va.LIB_PATH) & hooks)
+
+
+def _tree(lib, **over):
+    a = dict(tok=A16, lp=A16, B=2, D=4, K=3, T=8, free=A16, cap=100, head=A16, par=A16,
+             dtok=A16, depth=A16, loc=A16, status=None, stream=None)
+    a.update(over)
+    return lib.va_tree_build(a["tok"], a["lp"], a["B"], a["D"], a["K"], a["T"], a["free"],
+                             a["cap"], a["head"], a["par"], a["dtok"], a["depth"], a["loc"],
+                             a["status"], a["stream"])
+
+
+def test_tree_build_rejects_bad_arguments_before_any_launch(lib):
+    assert _tree(lib, tok=None) == -1
+    assert _tree(lib, par=None) == -1
+    assert _tree(lib, head=None) == -1            # a free list needs its head
+    assert _tree(lib, loc=None) == -1
+    assert _tree(lib, D=16) == -2 and _tree(lib, D=0) == -2
+    assert _tree(lib, K=17) == -2 and _tree(lib, K=0) == -2
+    assert _tree(lib, T=65) == -2 and _tree(lib, T=0) == -2
+    assert _tree(lib, B=0) == -2
+    # the candidate tree must hold T nodes: K=2, D=3 has 2 + 4 + 8 = 14
+    assert _tree(lib, K=2, D=3, T=15) == -2
+    assert _tree(lib, K=1, D=4, T=5) == -2
+    assert _tree(lib, lp=A16 + 2) == -3
+    assert _tree(lib, loc=A16 + 1) == -3
