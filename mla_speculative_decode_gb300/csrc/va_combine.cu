@@ -163,6 +163,84 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   }
 }
 
+// Merge for few splits and many rows (nsplit <= kRowSplits, e.g. a batch of
+// requests at full H): one warp per (row, 128-column chunk), no shared memory
+// and no block-wide reductions.  Lane j < nsplit_eff holds split j's lse; the
+// warp forms the maximum, the sum and the weights with shuffles, every lane
+// loads its four columns of every split up front and sums them.  Same
+// arithmetic as combine_kernel (the split order is fixed, so the result is
+// deterministic).
+constexpr int kRowSplits = 16;
+constexpr int kRowWarps = 8;   // warps per CTA
+
+__global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) {
+  const int rows_total = p.B * p.rows_per_req;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int row = item >> 2, chunk = item & 3;
+  const bool live = row < rows_total;
+  const int b = live ? row / p.rows_per_req : 0;
+  // the request's split count from its bounds (inputs of the call, not
+  // results of the split-K kernel), before the wait
+  const int ne = live ? split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff : 0;
+  griddep_wait();   // the split-K kernel's partials are complete and visible
+  if (live) {
+    const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
+    const size_t sstride = size_t(rows_total) * kDv;
+    uint2 buf[kRowSplits];
+#pragma unroll
+    for (int s = 0; s < kRowSplits; ++s)
+      buf[s] = s < ne ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
+                      : make_uint2(0u, 0u);
+    const float ls = lane < ne ? p.part_lse[size_t(lane) * rows_total + row] : -INFINITY;
+    float m = ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = (m == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float L = m == -INFINITY ? -INFINITY : m + logf(z);
+    const float w = (L == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - L);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kRowSplits; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      if (s < ne) {
+        const float2 lo = bf16x2_to_float2(buf[s].x), hi = bf16x2_to_float2(buf[s].y);
+        acc.x = fmaf(ws, lo.x, acc.x);
+        acc.y = fmaf(ws, lo.y, acc.y);
+        acc.z = fmaf(ws, hi.x, acc.z);
+        acc.w = fmaf(ws, hi.y, acc.w);
+      }
+    }
+    uint2 packed;
+    packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+    packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+    *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + chunk * kCombineCols + lane * 4) = packed;
+    if (chunk == 0 && lane == 0) p.lse[row] = L;
+  }
+  if (p.cta_flags && item == 0) {
+    // tensor-core path: the call's status word is the OR of the status words
+    // of every split-K CTA that ran (splits past a request's effective count
+    // exit at once and write none)
+    const int rbs = (p.rows_per_req + 127) / 128;
+    uint32_t v = 0u;
+    for (int bb = 0; bb < p.B; ++bb) {
+      const int nb = split_range(req_info(p, bb, false).N, p.nsplit, 0).nsplit_eff;
+      const size_t base = size_t(bb) * rbs * p.nsplit;
+      for (int i = lane; i < rbs * nb * 2; i += 32) {
+        const int rb = i / (nb * 2), sp = (i / 2) % nb, rank = i & 1;
+        v |= p.cta_flags[((base + size_t(rb) * p.nsplit) + sp) * 2 + rank];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) *p.status = v;
+  }
+}
+
 constexpr int kDefragThreads = 256;
 
 // A warp moves four rows per round: the four source slots arrive with one
@@ -234,13 +312,16 @@ __global__ void __launch_bounds__(kDefragThreads)
 
 cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   const int rows_total = p.B * p.rows_per_req;
-  dim3 grid(unsigned(rows_total), unsigned(kDv / kCombineCols), 1u);
+  const bool by_rows = p.nsplit <= kRowSplits;
+  dim3 grid = by_rows ? dim3(unsigned((rows_total * (kDv / kCombineCols) + kRowWarps - 1) / kRowWarps),
+                             1u, 1u)
+                      : dim3(unsigned(rows_total), unsigned(kDv / kCombineCols), 1u);
   // launched with programmatic stream serialization: its blocks may be
   // scheduled as the split-K kernel's clusters retire and wait in-kernel
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.blockDim = dim3(by_rows ? kRowWarps * 32 : kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -248,7 +329,8 @@ cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  return by_rows ? cudaLaunchKernelEx(&cfg, combine_rows_kernel, p)
+                 : cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 cudaError_t launch_defrag(void* pool, int64_t num_slots, int64_t stride, const int32_t* src,

@@ -972,13 +972,16 @@ bool tc_supported(int, int, int) { return true; }
 // SM count strand an SM).  With few (row block, request) items, one wave of
 // clusters splits each item evenly.  With many (more than half a wave), one
 // split per item would leave clusters idle and let the longest request of a
-// ragged batch set the time, so the items are split into about three waves
-// of clusters instead.  (Prefix lengths live on the device, so the rule uses
-// the shape only; splits past a request's keys exit at once.)
+// ragged batch set the time, so the items are split into about five and a
+// half waves of clusters instead (measured on 8 requests at H=64 with
+// prefixes from 13k to 46k keys: 3, 4, 5, 6, 7, 8, 10 splits per item ->
+// 727, 734, 693, 691, 669, 678, 700 us per step).  (Prefix lengths live on
+// the device, so the rule uses the shape only; splits past a request's keys
+// exit at once.)
 int tc_auto_nsplit(int B, int T, int H, int pairs) {
   const long rowblocks = (long(T) * H + kRows - 1) / kRows;
   const long items = rowblocks * B;
-  long ns = 2 * items <= pairs ? pairs / items : (3 * pairs + items - 1) / items;
+  long ns = 2 * items <= pairs ? pairs / items : (11 * pairs + 2 * items - 1) / (2 * items);
   if (ns < 1) ns = 1;
   if (ns > VA_NSPLIT_MAX) ns = VA_NSPLIT_MAX;
   return int(ns);
