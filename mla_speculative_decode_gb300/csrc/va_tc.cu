@@ -664,10 +664,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar(B_SEMPTY + bs));
+          // With a positive scale (the usual case) the raw scores are kept
+          // (hidden keys -inf), their maximum is scaled once, and each
+          // exponent below is one fused multiply-add (x * scale - m); a tile
+          // whose keys are all visible skips the mask.  Otherwise the scores
+          // are scaled here and the multiply-add's factor is 1.
+          if (p.scale_log2 > 0.f) {
+            if (v32 == 0xffffffffu) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x[c] = ((v32 >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-            mth = fmaxf(mth, x[c]);
+              for (int c = 0; c < 32; ++c) {
+                x[c] = __uint_as_float(sv[c]);
+                mth = fmaxf(mth, x[c]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                x[c] = ((v32 >> c) & 1u) ? __uint_as_float(sv[c]) : -INFINITY;
+                mth = fmaxf(mth, x[c]);
+              }
+            }
+            mth *= p.scale_log2;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              x[c] = ((v32 >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+              mth = fmaxf(mth, x[c]);
+            }
           }
         }
         VA_PH(1);
@@ -687,10 +709,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_ref = mt;
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+        const float sc = p.scale_log2 > 0.f ? p.scale_log2 : 1.f;
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16(ex2_approx(x[2 * c] - mr), ex2_approx(x[2 * c + 1] - mr), l);
+          pk[c] = pack_bf16(ex2_approx(fmaf(x[2 * c], sc, -mr)),
+                            ex2_approx(fmaf(x[2 * c + 1], sc, -mr)), l);
         if (tid == 128) VA_TRACE_EVENT(2, 1, t);
         VA_PH(3);
         // this row's 32 keys into the staging buffer (K-major, 128B swizzle)

@@ -568,3 +568,20 @@ def test_prepared_call_relaunches_on_new_contents(va):
     assert out2.data_ptr() == out.data_ptr()
     ref_o, ref_l = _gpu.reference(w2)
     _gpu.compare(out2, lse2, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("scale", [0.0, -0.0721, 0.31])
+def test_scale_sign(va, path, scale):
+    """The tensor-core softmax keeps raw scores and scales their maximum when
+    the scale is positive, and scales every score otherwise: both branches,
+    and a scale of zero (every visible key weighs the same), against the
+    oracle, with whole 64-key tiles and a ragged one."""
+    s = synth.Spec("scale", B=2, H=8, T=16, prefix=[900, 131], num_slots=8192, seed=97,
+                   sm_scale=scale)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=path, nsplit=3)
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
