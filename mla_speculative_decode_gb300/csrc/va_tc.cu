@@ -14,18 +14,18 @@
 //     ring of 23 slots of 8 KB, one 64-column block of a tile per slot, in the
 //     128B-swizzled K-major layout (16-byte cp.async gathers for paged keys,
 //     TMA boxes for contiguous ones); warp 1 issues S = Q K^T (36 MMAs of
-//     128x64x16, A from TMEM, B K-major) and releases each slot as soon as its
-//     four products are done; warps 4-11 are two softmax warpgroups, each
+//     128x64x16, A from TMEM, B K-major) with two commits per tile (blocks
+//     0-3 read, then S ready); warps 4-11 are two softmax warpgroups, each
 //     owning 32 of a tile's 64 columns for every row: they share the tile
 //     maximum through shared memory, run an online softmax with a conditional
 //     rescale (the reference max only moves when a tile exceeds it by 2^8),
 //     round P to bf16 into a local staging buffer, and one thread ships P with
 //     the rows' rescale factors to the PV CTA with a single
-//     distributed-shared-memory bulk copy.
+//     distributed-shared-memory bulk copy into a ring of three P buffers.
 //   PV CTA (cluster rank 1)
 //     TMEM: O (128 lanes x 512 columns fp32).  Warps 0, 2, 3, 12-15 bring the
 //     value columns (first 512) of the same tiles -- L2 hits behind the QK
-//     CTA's reads -- into a ring of 16 slots; warp 1 issues O += P V (8 MMAs
+//     CTA's reads -- into a ring of 20 slots; warp 1 issues O += P V (8 MMAs
 //     of 128x256x16, A = P K-major, B = V MN-major: the same swizzled block
 //     layout is K-major for S and MN-major for PV); warps 4-11 rescale O rows
 //     on the rare tiles whose reference max moved, then normalise and write
