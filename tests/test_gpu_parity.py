@@ -585,3 +585,19 @@ def test_scale_sign(va, path, scale):
     out, lse = _gpu.run(va, d, w, path=path, nsplit=3)
     ref_o, ref_l = _gpu.reference(w)
     _gpu.compare(out, lse, ref_o, ref_l)
+
+
+def test_many_small_requests(va):
+    """300 requests of 0-200 prefix keys (H=4, T=4): a grid of 300 requests
+    deep, a split count near 1 and the warp-per-row merge, every row against
+    the oracle."""
+    g = torch.Generator().manual_seed(123)
+    pre = [int(x) for x in torch.randint(0, 201, (300,), generator=g)]
+    s = synth.Spec("many", B=300, H=4, T=4, prefix=pre, num_slots=1 << 16, seed=124)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    ws, ns = va.alloc_workspace(s.B, s.T, s.H)
+    out, lse = _gpu.run(va, d, w, nsplit=ns, workspace=ws)
+    assert va.read_status(ws) == 0
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)

@@ -50,6 +50,7 @@ def _candidates(rng, B, D, K, kind):
     (3, 8, 1, 8, "dirichlet"),      # one candidate per depth: a chain
     (1, 1, 16, 16, "specials"),     # one depth: the candidates in order
     (2, 5, 4, 1, "dirichlet"),
+    (200, 8, 8, 16, "dirichlet"),   # many requests: 25 rounds of the CTA's warps
 ])
 def test_tree_build_matches_oracle(va, B, D, K, T, kind):
     rng = np.random.default_rng(B * 1000 + D * 10 + K)
