@@ -80,7 +80,10 @@ typedef struct CUstream_st *va_stream_t;
 /* Compute-path selection for the verify entry points (`flags`). */
 #define VA_PATH_AUTO 0  /* library's choice                                     */
 #define VA_PATH_FMA  1  /* CUDA-core FMA path (any shape)                       */
-#define VA_PATH_TC   2  /* tcgen05 tensor-core path                             */
+#define VA_PATH_TC   2  /* tcgen05 tensor-core path (two-SM products, M = 256,
+                           once a request has more than 128 rows)            */
+#define VA_PATH_TC_1SM 3 /* tensor-core path with one-SM products (M = 128) at
+                           every row count                                   */
 
 /* Library ABI version (major * 100 + minor). */
 int va_version(void);
@@ -107,9 +110,9 @@ int va_auto_nsplit(int B, int T, int H, int flags);
  * arithmetic, no CUDA call.  Layout (each region 256-byte aligned):
  *   [0, 256)        status word (uint32) and reserved header
  *   tree masks      uint64 [B*T]
- *   CTA status      uint32 [B][ceil(T*H/128)][nsplit][2] (tensor-core path:
- *                   each split-K CTA's status bits, OR-ed into the status
- *                   word by the merge)
+ *   CTA status      uint32 [B][2*ceil(T*H/256)][nsplit][2] (tensor-core
+ *                   path: each split-K CTA's status bits, OR-ed into the
+ *                   status word by the merge)
  *   partial lse     float  [nsplit][B*T*H]
  *   partial out     bf16   [nsplit][B*T*H][512] (normalised by the split's
  *                   row sum; merged in fp32)

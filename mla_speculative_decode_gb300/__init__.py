@@ -32,7 +32,7 @@ STATUS_BAD_INDPTR = 0x4
 STATUS_TIMEOUT = 0x8
 STATUS_BAD_DST = 0x10
 STATUS_BAD_MASK = 0x20
-PATH_AUTO, PATH_FMA, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_FMA, PATH_TC, PATH_TC_1SM = 0, 1, 2, 3
 
 LIB_PATH = _build_mod.LIB
 

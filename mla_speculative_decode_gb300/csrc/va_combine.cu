@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
     __shared__ uint32_t acc;
     if (tid == 0) acc = 0u;
     __syncthreads();
-    const int rbs = (p.rows_per_req + 127) / 128;
+    const int rbs = p.flag_blocks;
     uint32_t v = 0u;
     for (int b = 0; b < p.B; ++b) {
       const int ne = split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff;
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) 
     // tensor-core path: the call's status word is the OR of the status words
     // of every split-K CTA that ran (splits past a request's effective count
     // exit at once and write none)
-    const int rbs = (p.rows_per_req + 127) / 128;
+    const int rbs = p.flag_blocks;
     uint32_t v = 0u;
     for (int bb = 0; bb < p.B; ++bb) {
       const int nb = split_range(req_info(p, bb, false).N, p.nsplit, 0).nsplit_eff;

@@ -29,7 +29,7 @@ __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / 
 // Workspace regions (byte offsets from the workspace base).
 struct WsLayout {
   size_t bits;   // uint64 [B*T]
-  size_t flags;  // uint32 [B][row blocks of 128][nsplit][2]: status bits of each split-K CTA
+  size_t flags;  // uint32 [B][2 x row units of 256][nsplit][2]: status bits of each split-K CTA
   size_t plse;   // float  [nsplit][rows]
   size_t po;     // bf16   [nsplit][rows][512]
   size_t total;
@@ -40,7 +40,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int H, int nsplit) {
   const size_t rows = size_t(B) * T * H;
   L.bits = kHeaderBytes;
   L.flags = L.bits + align256(size_t(B) * T * sizeof(uint64_t));
-  const size_t rbs = (size_t(T) * H + 127) / 128;
+  const size_t rbs = 2 * ((size_t(T) * H + 255) / 256);   // 128-row blocks, rounded to pairs
   L.plse = L.flags + align256(size_t(B) * rbs * nsplit * 2 * sizeof(uint32_t));
   L.po = L.plse + align256(size_t(nsplit) * rows * sizeof(float));
   L.total = L.po + align256(size_t(nsplit) * rows * kDv * sizeof(__nv_bfloat16));
@@ -76,6 +76,8 @@ struct Params {
   // *status, so no kernel has to clear *status first.  NULL on the FMA path,
   // where the mask kernel clears *status and the kernels OR into it.
   uint32_t* cta_flags;
+  int flag_blocks;             // 128-row blocks of status words per request
+  int tc_pair;                 // tensor-core path: two-SM products (clusters of 4)
   __nv_bfloat16* out;          // [rows, 512]
   float* lse;                  // [rows]
 };

@@ -14,9 +14,11 @@
 
 namespace va {
 cudaError_t init_partial_fma();
-cudaError_t init_partial_tc(int* max_pairs);
+cudaError_t init_partial_tc(int* max_pairs, int* max_quads);
 bool tc_supported(int B, int T, int H);
-int tc_auto_nsplit(int B, int T, int H, int pairs);
+bool tc_use_pair(int T, int H, int flags);
+int tc_auto_nsplit(int B, int T, int H, int clusters, bool pair);
+int tc_flag_blocks(int T, int H, bool pair);
 cudaError_t launch_partial_tc(const Params& p, int num_sms, cudaStream_t st);
 }  // namespace va
 
@@ -27,6 +29,7 @@ struct DeviceState {
   int ready;
   int num_sms;
   int tc_pairs;   // two-CTA clusters of the tensor-core kernel resident at once
+  int tc_quads;   // four-CTA clusters (two-SM products) resident at once
 };
 DeviceState g_dev[kMaxDevices];   // written by va_init only
 cudaEvent_t g_ev_before = nullptr; // benchmark timing hook (va_set_partial_events)
@@ -62,8 +65,15 @@ int auto_nsplit_fma(int B, int T, int H, int num_sms) {
 
 int pick_path(int flags, int B, int T, int H) {
   if (flags == VA_PATH_FMA) return VA_PATH_FMA;
-  if (flags == VA_PATH_TC) return va::tc_supported(B, T, H) ? VA_PATH_TC : -1;
+  if (flags == VA_PATH_TC || flags == VA_PATH_TC_1SM)
+    return va::tc_supported(B, T, H) ? VA_PATH_TC : -1;
   return va::tc_supported(B, T, H) ? VA_PATH_TC : VA_PATH_FMA;
+}
+
+int auto_nsplit(const DeviceState& ds, int path, int flags, int B, int T, int H) {
+  if (path != VA_PATH_TC) return auto_nsplit_fma(B, T, H, ds.num_sms);
+  const bool pair = va::tc_use_pair(T, H, flags);
+  return va::tc_auto_nsplit(B, T, H, pair ? ds.tc_quads : ds.tc_pairs, pair);
 }
 
 // Shared by the entry points.  Key addressing: kv_start (contiguous rows),
@@ -88,7 +98,7 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   if (int64_t(B) * T * H > (int64_t(1) << 24)) return VA_ERR_SHAPE;
   if (num_slots < 1 || stride < VA_D_QK) return VA_ERR_SHAPE;
   if (nsplit < 0 || nsplit > VA_NSPLIT_MAX) return VA_ERR_SHAPE;
-  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC) return VA_ERR_SHAPE;
+  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC_1SM) return VA_ERR_SHAPE;
   if (!isfinite(sm_scale)) return VA_ERR_SHAPE;
   if (stride % 8 != 0) return VA_ERR_ALIGN;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(ws, 256) ||
@@ -111,8 +121,7 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   if (path < 0) return VA_ERR_UNSUPPORTED;
   int ns = nsplit;
   if (ns == 0)
-    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
-                            : auto_nsplit_fma(B, T, H, ds.num_sms);
+    ns = auto_nsplit(ds, path, flags, B, T, H);
   const va::WsLayout L = va::ws_layout(B, T, H, ns);
   if (ws_bytes < L.total) return VA_ERR_WORKSPACE;
 
@@ -150,7 +159,11 @@ int verify_common(const void* q, const void* kv, int64_t num_slots, int64_t stri
   // per-CTA status words that the merge combines, so the mask kernel runs
   // there only to append draft rows.  The FMA path reads the masks the mask
   // kernel writes, and the mask kernel clears the status word for it.
-  if (path == VA_PATH_TC) p.cta_flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  if (path == VA_PATH_TC) {
+    p.cta_flags = reinterpret_cast<uint32_t*>(w + L.flags);
+    p.tc_pair = va::tc_use_pair(T, H, flags) ? 1 : 0;
+    p.flag_blocks = va::tc_flag_blocks(T, H, p.tc_pair != 0);
+  }
   if (path != VA_PATH_TC || p.draft_kv) {
     if (va::launch_tree_bits(p, reinterpret_cast<uint64_t*>(w + L.bits), st) != cudaSuccess)
       return VA_ERR_LAUNCH;
@@ -200,8 +213,8 @@ VA_API int va_init(int device) {
   if (cudaGetDevice(&prev) != cudaSuccess) return VA_ERR_CUDA;
   if (cudaSetDevice(device) != cudaSuccess) return VA_ERR_CUDA;
   cudaError_t e1 = va::init_partial_fma();
-  int pairs = 0;
-  cudaError_t e2 = va::init_partial_tc(&pairs);
+  int pairs = 0, quads = 0;
+  cudaError_t e2 = va::init_partial_tc(&pairs, &quads);
   // the no-allocation scratch array: placed now, with the device current; a
   // failure here (no memory left for it) is not an error of va_init -- the
   // first verify_attn_paged_noalloc call on the device retries and reports it
@@ -210,20 +223,20 @@ VA_API int va_init(int device) {
   if (e1 != cudaSuccess || e2 != cudaSuccess) return VA_ERR_CUDA;
   g_dev[device].num_sms = prop.multiProcessorCount;
   g_dev[device].tc_pairs = pairs > 0 ? pairs : prop.multiProcessorCount / 2;
+  g_dev[device].tc_quads = quads > 0 ? quads : prop.multiProcessorCount / 4;
   g_dev[device].ready = 1;
   return VA_OK;
 }
 
 VA_API int va_auto_nsplit(int B, int T, int H, int flags) {
   if (B < 1 || T < 1 || T > VA_T_MAX || H < 1) return VA_ERR_SHAPE;
-  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC) return VA_ERR_SHAPE;
+  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC_1SM) return VA_ERR_SHAPE;
   DeviceState ds;
   int rc = current_state(&ds);
   if (rc != VA_OK) return rc;
   const int path = pick_path(flags, B, T, H);
   if (path < 0) return VA_ERR_UNSUPPORTED;
-  return path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
-                            : auto_nsplit_fma(B, T, H, ds.num_sms);
+  return auto_nsplit(ds, path, flags, B, T, H);
 }
 
 VA_API size_t va_workspace_bytes(int B, int T, int H, int nsplit) {
@@ -303,7 +316,7 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
                                      void* out, float* lse, va_stream_t stream) {
   if (B < 1 || T < 1 || T > VA_T_MAX || H < 1 || nsplit < 0 || nsplit > VA_NSPLIT_MAX)
     return VA_ERR_SHAPE;
-  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC) return VA_ERR_SHAPE;
+  if (flags < VA_PATH_AUTO || flags > VA_PATH_TC_1SM) return VA_ERR_SHAPE;
   const size_t cap = VA_NOALLOC_SCRATCH_BYTES;
   // an explicit split count that does not fit is rejected before any CUDA call
   if (nsplit > 0 && va::ws_layout(B, T, H, nsplit).total > cap) return VA_ERR_WORKSPACE;
@@ -319,8 +332,7 @@ VA_API int verify_attn_paged_noalloc(const void* q, const void* kv_pool, int64_t
   if (ns == 0) {
     const int path = pick_path(flags, B, T, H);
     if (path < 0) return VA_ERR_UNSUPPORTED;
-    ns = path == VA_PATH_TC ? va::tc_auto_nsplit(B, T, H, ds.tc_pairs)
-                            : auto_nsplit_fma(B, T, H, ds.num_sms);
+    ns = auto_nsplit(ds, path, flags, B, T, H);
     while (ns > 1 && va::ws_layout(B, T, H, ns).total > cap) --ns;
   }
   if (va::ws_layout(B, T, H, ns).total > cap) return VA_ERR_WORKSPACE;

@@ -36,6 +36,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Arrive on an mbarrier of another CTA of the cluster without release
+// ordering: for a signal that publishes no memory writes (e.g. "these tensor
+// memory loads have completed", after tcgen05.wait::ld), at a fraction of the
+// cost of a cluster-scope release.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
 // Non-suspending phase test: the waiter polls, so a phase completed by
 // another SM is seen at once.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -296,6 +305,23 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Pair forms (cta_group::2): the CTAs of cluster ranks 2k and 2k+1 allocate
+// the same columns of their own tensor memory together (one warp of each CTA
+// makes the call), and the even rank issues products of M = 256 rows for
+// both: each CTA holds its own 128 rows of A and of the accumulator, at the
+// same TMEM column or shared-memory offset, and half of B (the first or the
+// second half of its N extent).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 // D(tmem) (+)= A(smem desc) * B(smem desc)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -352,6 +378,35 @@ __device__ __forceinline__ void mma_commit_mc_warp(uint32_t bar, uint16_t cta_ma
       "h"(cta_mask)
       : "memory");
 }
+// Pair products and their completion (see tmem_alloc_pair): issued by the
+// even rank of the pair; the commit arrives on the barrier at the same
+// shared offset in every CTA of `cta_mask` once the products are complete in
+// both CTAs.
+__device__ __forceinline__ void mma2_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred e, p;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred e, p;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_commit_mc_warp(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;\n}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Lane-elected single arrive / expect_tx for a converged warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

@@ -61,7 +61,7 @@ def test_workspace_bytes_layout(lib):
     B, T, H, ns = 2, 16, 8, 5
     rows = B * T * H
     al = lambda x: (x + 255) // 256 * 256
-    rbs = (T * H + 127) // 128
+    rbs = 2 * ((T * H + 255) // 256)   # 128-row blocks, rounded up to pairs
     want = 256 + al(B * T * 8) + al(B * rbs * ns * 2 * 4) + al(ns * rows * 4) + al(ns * rows * 512 * 2)
     assert va.workspace_bytes(B, T, H, ns) == want
     assert lib.va_workspace_bytes(0, 16, 8, 1) == 0

@@ -14,7 +14,7 @@ from tests import _gpu
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"fma": 1, "tc": 2}
+PATHS = {"fma": 1, "tc": 2, "tc1sm": 3}
 
 
 @pytest.fixture(scope="module")
@@ -28,7 +28,7 @@ def va():
 
 
 def _need(va, path, B, T, H):
-    if path == PATHS["tc"]:
+    if path in (PATHS["tc"], PATHS["tc1sm"]):
         try:
             va.auto_nsplit(B, T, H, path)
         except va.VaError as e:

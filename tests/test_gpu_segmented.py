@@ -17,7 +17,7 @@ from tests.test_oracle_pins import _dense_mask
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"fma": 1, "tc": 2}
+PATHS = {"fma": 1, "tc": 2, "tc1sm": 3}
 
 
 @pytest.fixture(scope="module")

@@ -40,10 +40,13 @@ def libs():
     th.va_test_set_gate(None)
 
 
+# H=8: one 128-row block per request (one-SM products, clusters of two);
+# H=32: 512 rows per request (two-SM products, clusters of four)
+@pytest.mark.parametrize("H", [8, 32])
 @pytest.mark.parametrize("layout", ["scattered", "contiguous"])
-def test_wait_that_runs_out_sets_timeout_and_the_next_call_is_correct(libs, layout):
+def test_wait_that_runs_out_sets_timeout_and_the_next_call_is_correct(libs, layout, H):
     va, th = libs
-    s = synth.Spec("to", B=2, H=8, T=16, prefix=[3000, 700], num_slots=1 << 14, layout=layout,
+    s = synth.Spec("to", B=2, H=H, T=16, prefix=[3000, 700], num_slots=1 << 14, layout=layout,
                    seed=91)
     w = synth.make(s)
     d = _gpu.to_device(w)
