@@ -54,6 +54,21 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
+// The call's status word on the tensor-core path: the OR of the status words
+// of every split-K CTA of the grid (a CTA past its request's splits stores
+// 0), loaded by a whole block, four independent loads in flight per thread.
+__device__ __forceinline__ uint32_t cta_flags_or(const Params& p, int tid, int nthreads) {
+  const size_t n = size_t(p.B) * p.flag_blocks * p.nsplit * 2;
+  const size_t step = size_t(nthreads);
+  uint32_t v = 0u;
+  size_t i = size_t(tid);
+  for (; i + 3 * step < n; i += 4 * step)
+    v |= p.cta_flags[i] | p.cta_flags[i + step] | p.cta_flags[i + 2 * step] |
+         p.cta_flags[i + 3 * step];
+  for (; i < n; i += step) v |= p.cta_flags[i];
+  return v;
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   __shared__ float wsplit[kMaxSplits];
   __shared__ float red[kCombineThreads / 32];
@@ -141,22 +156,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
     if (chunk == 0 && lane == 0) p.lse[row] = L;
   }
   if (p.cta_flags && row == 0 && chunk == 0) {
-    // tensor-core path: the call's status word is the OR of the status words
-    // of every split-K CTA that ran (splits past a request's effective count
-    // exit at once and write none)
     __shared__ uint32_t acc;
     if (tid == 0) acc = 0u;
     __syncthreads();
-    const int rbs = p.flag_blocks;
-    uint32_t v = 0u;
-    for (int b = 0; b < p.B; ++b) {
-      const int ne = split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff;
-      const size_t base = size_t(b) * rbs * p.nsplit;
-      for (int i = tid; i < rbs * ne * 2; i += kCombineThreads) {
-        const int rb = i / (ne * 2), s = (i / 2) % ne, rank = i & 1;
-        v |= p.cta_flags[((base + size_t(rb) * p.nsplit) + s) * 2 + rank];
-      }
-    }
+    const uint32_t v = cta_flags_or(p, tid, kCombineThreads);
     if (v) atomicOr(&acc, v);
     __syncthreads();
     if (tid == 0) *p.status = acc;
@@ -221,23 +224,16 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) 
     *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + chunk * kCombineCols + lane * 4) = packed;
     if (chunk == 0 && lane == 0) p.lse[row] = L;
   }
-  if (p.cta_flags && item == 0) {
-    // tensor-core path: the call's status word is the OR of the status words
-    // of every split-K CTA that ran (splits past a request's effective count
-    // exit at once and write none)
-    const int rbs = p.flag_blocks;
-    uint32_t v = 0u;
-    for (int bb = 0; bb < p.B; ++bb) {
-      const int nb = split_range(req_info(p, bb, false).N, p.nsplit, 0).nsplit_eff;
-      const size_t base = size_t(bb) * rbs * p.nsplit;
-      for (int i = lane; i < rbs * nb * 2; i += 32) {
-        const int rb = i / (nb * 2), sp = (i / 2) % nb, rank = i & 1;
-        v |= p.cta_flags[((base + size_t(rb) * p.nsplit) + sp) * 2 + rank];
-      }
-    }
+  if (p.cta_flags && blockIdx.x == 0) {
+    __shared__ uint32_t acc;
+    if (threadIdx.x == 0) acc = 0u;
+    __syncthreads();
+    uint32_t v = cta_flags_or(p, threadIdx.x, kRowWarps * 32);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) *p.status = v;
+    if (lane == 0 && v) atomicOr(&acc, v);
+    __syncthreads();
+    if (threadIdx.x == 0) *p.status = acc;
   }
 }
 

@@ -562,7 +562,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before a tile holding draft keys.
   const ReqInfo ri = req_info(p, b, false);
   const SplitRange sr = split_range(ri.N, p.nsplit, split);
-  if (split >= sr.nsplit_eff) return;   // every CTA of the cluster leaves together
+  // this CTA's status word, for the merge kernel to OR into the status word
+  // (words [request][128-row block][split][QK, PV]; every CTA of the grid
+  // owns one and stores it, so the merge ORs them all without bounds)
+  uint32_t* const flag_word =
+      p.cta_flags +
+      ((size_t(b) * p.flag_blocks + (kPair ? 2 * rb + hh : rb)) * p.nsplit + split) * 2 + (qk ? 0 : 1);
+  if (split >= sr.nsplit_eff) {   // every CTA of the cluster leaves together
+    if (threadIdx.x == 0) *flag_word = 0u;
+    return;
+  }
   const int R = p.rows_per_req;
   const int row0 = rb * C::kUnitRows + hh * kRows;
   const int ntiles = ceil_div(sr.k1 - sr.k0, kTile);
@@ -1199,13 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 2);
   tc_fence_before();
   __syncthreads();
-  // this CTA's status bits, for the merge kernel to OR into the status word
-  // (words [request][128-row block][split][QK, PV])
-  if (tid == 0) {
-    const int blk = kPair ? 2 * rb + hh : rb;
-    p.cta_flags[((size_t(b) * p.flag_blocks + blk) * p.nsplit + split) * 2 + (qk ? 0 : 1)] =
-        *cta_flags;
-  }
+  if (tid == 0) *flag_word = *cta_flags;   // this CTA's status bits
   if (tid == 0) VA_TRACE_CTA(6 + int(rank), 3);
   if constexpr (kPair) {
     // Every CTA of the cluster has finished every role before any frees its

@@ -71,6 +71,12 @@ SWEEP = [
     (1, 24, 10, [3000], "random", 0),
     (2, 40, 7, [100, 2500], "random", 3),
     (1, 128, 2, [700], "flat", 0),
+    # just over one 128-row block: two-SM products whose second half is
+    # mostly (129 rows) or partly (136) padding, and 1.5 units of 256 rows
+    # with 40 splits of two tiles each
+    (1, 43, 3, [300], "random", 0),
+    (2, 8, 17, [150, 1400], "chain", 0),
+    (1, 24, 16, [5000], "random", 40),
     # many short requests: the split rule's several-waves regime
     (16, 8, 4, [0, 5, 64, 65, 127, 128, 129, 300, 1, 2, 3, 511, 512, 513, 40, 90], "random", 0),
 ]
