@@ -195,41 +195,63 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 #ifdef VA_TRACE
+// Trace build only.  The buffer g_va_trace holds 18 roles x 8 slots x 512
+// entries; only the grid's first (row unit, request) column is traced:
+//   roles 0-4   per-tile events of cluster 0: key producers, QK products,
+//               softmax, value producers, PV products (the first CTA of each
+//               role: cluster ranks 0 and 1, or 0 and 2 in a pair);
+//   role 5      write-out marks; roles 6-7 and 16-17 per-CTA marks by
+//               cluster rank (0-1, 2-3);
+//   roles 8-12  phase clock sums per cluster: softmax, QK products, PV
+//               products, key producers, value producers (13-15: softmax
+//               and producers of a pair's odd ranks).
+__device__ __forceinline__ unsigned va_trace_cluster() {
+  unsigned n;
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return blockIdx.x / n;
+}
+__device__ __forceinline__ bool va_trace_first_of_role() {
+  unsigned r, n;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return r == 0 || 2 * r == n;
+}
 #ifdef VA_TRACE_NO_EVENTS
 #define VA_TRACE_EVENT(role, ev, t) ((void)0)
 #else
 #define VA_TRACE_EVENT(role, ev, t)                                                        \
-  do {                                                                                   \
-    if (g_va_trace && blockIdx.x < 2 && blockIdx.y == 0 && blockIdx.z == 0 && (t) < 512) { \
-      unsigned long long _ts;                                                             \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                              \
-      g_va_trace[((role) * 8 + (ev)) * 512 + (t)] = _ts;                                  \
-    }                                                                                    \
+  do {                                                                                     \
+    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && va_trace_cluster() == 0 &&       \
+        va_trace_first_of_role() && (t) < 512) {                                           \
+      unsigned long long _ts;                                                              \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                               \
+      g_va_trace[((role) * 8 + (ev)) * 512 + (t)] = _ts;                                   \
+    }                                                                                      \
   } while (0)
 #endif
 // Per-cluster marks of the partial kernel: slot (role, ev, cluster index).
 #define VA_TRACE_CTA(role, ev)                                                             \
   do {                                                                                     \
-    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && (blockIdx.x >> 1) < 512) {       \
-      unsigned long long _ts;                                                               \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                                \
-      g_va_trace[((role) * 8 + (ev)) * 512 + (blockIdx.x >> 1)] = _ts;                      \
+    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && va_trace_cluster() < 512) {     \
+      unsigned long long _ts;                                                              \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_ts));                               \
+      g_va_trace[((role) * 8 + (ev)) * 512 + va_trace_cluster()] = _ts;                    \
     }                                                                                      \
   } while (0)
 // Phase clocks: a role accumulates clock64 deltas per phase over all tiles
-// in registers and stores the sums once, into roles 8-15 of the buffer.
+// in registers and stores the sums once.
 #define VA_PH_DECL long long _ph[8] = {0, 0, 0, 0, 0, 0, 0, 0}; long long _pt = clock64()
 #define VA_PH(i)                                                                           \
   do {                                                                                     \
     const long long _n = clock64();                                                        \
-    _ph[i] += _n - _pt;                                                                     \
+    _ph[i] += _n - _pt;                                                                    \
     _pt = _n;                                                                              \
   } while (0)
 #define VA_PH_STORE(role)                                                                  \
   do {                                                                                     \
-    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && (blockIdx.x >> 1) < 512)       \
+    if (g_va_trace && blockIdx.y == 0 && blockIdx.z == 0 && va_trace_cluster() < 512)       \
       for (int _i = 0; _i < 8; ++_i)                                                       \
-        g_va_trace[((role) * 8 + _i) * 512 + (blockIdx.x >> 1)] = (unsigned long long)_ph[_i]; \
+        g_va_trace[((role) * 8 + _i) * 512 + va_trace_cluster()] = (unsigned long long)_ph[_i]; \
   } while (0)
 #else
 #define VA_TRACE_EVENT(role, ev, t) ((void)0)

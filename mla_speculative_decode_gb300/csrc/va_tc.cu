@@ -469,7 +469,7 @@ __device__ __forceinline__ bool produce(const Params& p, const ReqInfo& ri, cons
     if (ptid == 0) VA_TRACE_EVENT(kMask ? 0 : 3, 1, t);
     VA_PH(2);
   }
-  if (ptid == 0) VA_PH_STORE(kMask ? 11 : 12);
+  if (ptid == 0) VA_PH_STORE((kMask ? 11 : 12) + 3 * hh);
   cp_async_wait_all();
   // After a wait gave up, the boxes still in flight land before the CTA can
   // leave.  Each full barrier's last issued tile received all of its
@@ -543,7 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mate = rank ^ 1u;
   const int split = blockIdx.x / C::kCtas, rb = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 0);
+#ifdef VA_TRACE
+  const int trace_role = rank < 2u ? 6 + int(rank) : 14 + int(rank);   // per-CTA marks
+#endif
+  if (tid == 0) VA_TRACE_CTA(trace_role, 0);
   // the maps' descriptors are fetched while the request's bounds load
   if (tid == 0) {
     if (qk) tma_prefetch(&tmap_q);
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + C::kOffTmemSlot);
-  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 1);
+  if (tid == 0) VA_TRACE_CTA(trace_role, 1);
   int* srow = reinterpret_cast<int*>(gb + C::kOffSrow);
   const int half = (warp - 4) >> 2;   // softmax / row warpgroup (warps >= 4)
   const int q4 = warp & 3;            // TMEM lane quadrant of the warp
@@ -927,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         VA_PH(6);
       }
-      if (tid == 128) VA_PH_STORE(8);
+      if (tid == 128) VA_PH_STORE(8 + 5 * hh);
       // row sums: the two warpgroups' partial sums share the reference max
       if (ok) {
         mx[half * kRows + r] = l;
@@ -1205,11 +1208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 2);
+  if (tid == 0) VA_TRACE_CTA(trace_role, 2);
   tc_fence_before();
   __syncthreads();
   if (tid == 0) *flag_word = *cta_flags;   // this CTA's status bits
-  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 3);
+  if (tid == 0) VA_TRACE_CTA(trace_role, 3);
   if constexpr (kPair) {
     // Every CTA of the cluster has finished every role before any frees its
     // tensor memory or leaves: a pair's products read and write both CTAs'
@@ -1236,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       cluster_wait();
   }
-  if (tid == 0) VA_TRACE_CTA(6 + int(rank), 4);
+  if (tid == 0) VA_TRACE_CTA(trace_role, 4);
 }
 
 // Clusters of `ctas` CTAs of the kernel that the device runs at once.
