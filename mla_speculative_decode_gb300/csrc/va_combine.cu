@@ -167,20 +167,45 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 }
 
 // Merge for few splits and many rows (nsplit <= kRowSplits, e.g. a batch of
-// requests at full H): one warp per (row, 128-column chunk), no shared memory
-// and no block-wide reductions.  Lane j < nsplit_eff holds split j's lse; the
-// warp forms the maximum, the sum and the weights with shuffles, every lane
-// loads its four columns of every split up front and sums them.  Same
-// arithmetic as combine_kernel (the split order is fixed, so the result is
-// deterministic).
+// requests at full H): one warp per (row, 32*kVec-column chunk), no shared
+// memory and no block-wide reductions.  Lane j < nsplit_eff holds split j's
+// lse; the warp forms the maximum, the sum and the weights with shuffles;
+// every lane loads its kVec columns of every split up front (while the
+// weights are formed) and sums them.  The launch sizes the split buffer to
+// the split count: up to 8 splits, 16-byte lanes (kVec = 8); 9 to 16, 8-byte
+// lanes (kVec = 4), so that the buffer stays small enough for the warps that
+// keep the loads in flight.  Same arithmetic as combine_kernel (the split
+// order is fixed, so the result is deterministic).
 constexpr int kRowSplits = 16;
-constexpr int kRowWarps = 8;   // warps per CTA
+constexpr int kRowWarps = 8;    // warps per CTA
 
+template <int kVec>
+struct RowVec;
+template <>
+struct RowVec<8> {
+  using T = uint4;
+  __device__ static uint32_t word(const uint4& v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+  }
+  __device__ static uint4 zero() { return make_uint4(0u, 0u, 0u, 0u); }
+  __device__ static uint4 make(const uint32_t* w) { return make_uint4(w[0], w[1], w[2], w[3]); }
+};
+template <>
+struct RowVec<4> {
+  using T = uint2;
+  __device__ static uint32_t word(const uint2& v, int k) { return k == 0 ? v.x : v.y; }
+  __device__ static uint2 zero() { return make_uint2(0u, 0u); }
+  __device__ static uint2 make(const uint32_t* w) { return make_uint2(w[0], w[1]); }
+};
+
+template <int kMax, int kVec>
 __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) {
+  using V = RowVec<kVec>;
+  constexpr int kChunks = kDv / (32 * kVec);   // warps per row
   const int rows_total = p.B * p.rows_per_req;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  const int row = item >> 2, chunk = item & 3;
+  const int row = item / kChunks, chunk = item % kChunks;
   const bool live = row < rows_total;
   const int b = live ? row / p.rows_per_req : 0;
   // the request's split count from its bounds (inputs of the call, not
@@ -188,13 +213,13 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) 
   const int ne = live ? split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff : 0;
   griddep_wait();   // the split-K kernel's partials are complete and visible
   if (live) {
-    const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
+    const size_t col = size_t(chunk) * (32 * kVec) + size_t(lane) * kVec;
+    const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + col;
     const size_t sstride = size_t(rows_total) * kDv;
-    uint2 buf[kRowSplits];
+    typename V::T buf[kMax];
 #pragma unroll
-    for (int s = 0; s < kRowSplits; ++s)
-      buf[s] = s < ne ? *reinterpret_cast<const uint2*>(po + size_t(s) * sstride)
-                      : make_uint2(0u, 0u);
+    for (int s = 0; s < kMax; ++s)
+      buf[s] = s < ne ? *reinterpret_cast<const typename V::T*>(po + size_t(s) * sstride) : V::zero();
     const float ls = lane < ne ? p.part_lse[size_t(lane) * rows_total + row] : -INFINITY;
     float m = ls;
 #pragma unroll
@@ -204,36 +229,39 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) 
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     const float L = m == -INFINITY ? -INFINITY : m + logf(z);
     const float w = (L == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - L);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[kVec];
 #pragma unroll
-    for (int s = 0; s < kRowSplits; ++s) {
+    for (int k = 0; k < kVec; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMax; ++s) {
       const float ws = __shfl_sync(0xffffffffu, w, s);
       if (s < ne) {
-        const float2 lo = bf16x2_to_float2(buf[s].x), hi = bf16x2_to_float2(buf[s].y);
-        acc.x = fmaf(ws, lo.x, acc.x);
-        acc.y = fmaf(ws, lo.y, acc.y);
-        acc.z = fmaf(ws, hi.x, acc.z);
-        acc.w = fmaf(ws, hi.y, acc.w);
+#pragma unroll
+        for (int k = 0; k < kVec / 2; ++k) {
+          const float2 f = bf16x2_to_float2(V::word(buf[s], k));
+          acc[2 * k] = fmaf(ws, f.x, acc[2 * k]);
+          acc[2 * k + 1] = fmaf(ws, f.y, acc[2 * k + 1]);
+        }
       }
     }
-    uint2 packed;
-    packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-    packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(p.out + size_t(row) * kDv + chunk * kCombineCols + lane * 4) = packed;
+    uint32_t pk[kVec / 2];
+#pragma unroll
+    for (int k = 0; k < kVec / 2; ++k)
+      pk[k] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k]))) |
+              (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k + 1]))) << 16);
+    *reinterpret_cast<typename V::T*>(p.out + size_t(row) * kDv + col) = V::make(pk);
     if (chunk == 0 && lane == 0) p.lse[row] = L;
   }
   if (p.cta_flags && blockIdx.x == 0) {
-    __shared__ uint32_t acc;
-    if (threadIdx.x == 0) acc = 0u;
+    __shared__ uint32_t acc_flags;
+    if (threadIdx.x == 0) acc_flags = 0u;
     __syncthreads();
     uint32_t v = cta_flags_or(p, threadIdx.x, kRowWarps * 32);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0 && v) atomicOr(&acc, v);
+    if (lane == 0 && v) atomicOr(&acc_flags, v);
     __syncthreads();
-    if (threadIdx.x == 0) *p.status = acc;
+    if (threadIdx.x == 0) *p.status = acc_flags;
   }
 }
 
@@ -309,7 +337,8 @@ __global__ void __launch_bounds__(kDefragThreads)
 cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   const int rows_total = p.B * p.rows_per_req;
   const bool by_rows = p.nsplit <= kRowSplits;
-  dim3 grid = by_rows ? dim3(unsigned((rows_total * (kDv / kCombineCols) + kRowWarps - 1) / kRowWarps),
+  const int row_vec = p.nsplit <= 8 ? 8 : 4;   // columns per lane of the warp-per-row merge
+  dim3 grid = by_rows ? dim3(unsigned((rows_total * (kDv / (32 * row_vec)) + kRowWarps - 1) / kRowWarps),
                              1u, 1u)
                       : dim3(unsigned(rows_total), unsigned(kDv / kCombineCols), 1u);
   // launched with programmatic stream serialization: its blocks may be
@@ -325,8 +354,10 @@ cudaError_t launch_combine(const Params& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return by_rows ? cudaLaunchKernelEx(&cfg, combine_rows_kernel, p)
-                 : cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  if (!by_rows) return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  if (p.nsplit <= 4) return cudaLaunchKernelEx(&cfg, combine_rows_kernel<4, 8>, p);
+  if (p.nsplit <= 8) return cudaLaunchKernelEx(&cfg, combine_rows_kernel<8, 8>, p);
+  return cudaLaunchKernelEx(&cfg, combine_rows_kernel<kRowSplits, 4>, p);
 }
 
 cudaError_t launch_defrag(void* pool, int64_t num_slots, int64_t stride, const int32_t* src,
