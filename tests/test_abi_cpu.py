@@ -86,6 +86,7 @@ def _paged(lib, **over):
     (dict(parent=None, bits=None), -1),
     (dict(B=0), -2), (dict(T=0), -2), (dict(T=65), -2), (dict(H=0), -2), (dict(num_slots=0), -2),
     (dict(stride=512), -2), (dict(nsplit=-1), -2), (dict(nsplit=1025), -2), (dict(flags=7), -2),
+    (dict(flags=4), -2), (dict(flags=-1), -2),
     (dict(scale=float("nan")), -2),
     (dict(stride=580), -3), (dict(q=A16 + 8), -3), (dict(kv=A16 + 2), -3), (dict(out=A16 + 4), -3),
     (dict(ws=A256 + 16), -3), (dict(lse=A16 + 2), -3), (dict(slot=A16 + 2), -3),
@@ -98,6 +99,11 @@ def test_paged_argument_errors(lib, over, code):
 def test_valid_arguments_without_gpu_do_not_crash(lib):
     # no device (or no va_init): an error code, never a crash
     rc = _paged(lib)
+    assert rc in (-5, -7)
+    # every compute-path flag passes the argument checks, the one-SM
+    # tensor-core shape (VA_PATH_TC_1SM = 3) included
+    for flags in (0, 1, 2, 3):
+        assert _paged(lib, flags=flags) in (-5, -7)
     assert rc in (-5, -7)
 
 
