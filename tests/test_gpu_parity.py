@@ -607,3 +607,27 @@ def test_many_small_requests(va):
     assert va.read_status(ws) == 0
     ref_o, ref_l = _gpu.reference(w)
     _gpu.compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("H,T,prefix,layout", [
+    (64, 16, [3000], "scattered"),
+    (64, 16, [2000, 5001], "contiguous"),
+    (24, 10, [1700], "scattered"),      # 240 rows: one unit, its second half partly padding
+    (8, 32, [900, 40], "scattered"),    # 256 rows
+])
+def test_tensor_core_shapes_agree(va, H, T, prefix, layout):
+    """Two-SM products (VA_PATH_TC at more than 128 rows) against one-SM
+    products (VA_PATH_TC_1SM) at the same split count: the same per-row
+    arithmetic in the same order, so the same bits; both also against the
+    oracle."""
+    s = synth.Spec("shapes", B=len(prefix), H=H, T=T, prefix=prefix, num_slots=1 << 15,
+                   layout=layout, seed=H * 7 + T)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    o2, l2 = _gpu.run(va, d, w, path=PATHS["tc"], nsplit=5)
+    o1, l1 = _gpu.run(va, d, w, path=PATHS["tc1sm"], nsplit=5)
+    torch.cuda.synchronize()
+    diff = (o2.float() - o1.float()).abs().max().item()
+    assert torch.equal(o2, o1) and torch.equal(l2, l1), f"max |out diff| {diff}"
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(o2, l2, ref_o, ref_l)
