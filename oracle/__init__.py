@@ -43,6 +43,16 @@ Functions and the passages they follow (page titles and sections):
                    draft tokens' own slots at out_cache_loc, and a custom mask
                    with one row per draft token of stride prefix + q_len;
                    out_cache_loc is where the draft tokens' KV goes).
+  append_contiguous, compact_accepted
+                -- The Checkpoint Report, "Input Knowledge Required" (KV
+                   defragmentation keeps per-request KV contiguous) and "The
+                   Architecture of the Report" (defragmentation, the deferred
+                   phase; its placement policy, "Tier 1 defrag", is named on
+                   the pages but not specified).  The reading: a request owns
+                   a reserved range of rows; its draft latents land right after
+                   its prefix, and after acceptance the accepted path's rows
+                   are moved to directly after the prefix, which grows by the
+                   accepted count.
 """
 from __future__ import annotations
 
@@ -400,3 +410,69 @@ def defrag(pool_bits, src_slots, src_indptr, dst_base):
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv))
+
+
+def append_contiguous(pool_bits, draft_bits, kv_start, prefix_len, capacity, T: int):
+    """Draft latents of request b into the rows after its prefix.
+
+    Node i of request b goes to row kv_start[b] + prefix_len[b] + i when the
+    request's reserved range of capacity[b] rows holds prefix and draft
+    (prefix_len[b] + T <= capacity[b]) and the row lies in the pool (and below
+    2^31); otherwise the node gets no row.  Returns (a copy of the pool with
+    draft_bits[b*T + i] written into the first columns of that row,
+    out_cache_loc int32 [B*T] with the row or -1, the number of nodes without
+    a row)."""
+    pool = np.array(pool_bits, dtype=np.uint16, copy=True, order="C")
+    draft = np.asarray(draft_bits, dtype=np.uint16)
+    ks = np.asarray(kv_start).reshape(-1).tolist()
+    pl = np.asarray(prefix_len).reshape(-1).tolist()
+    cap = np.asarray(capacity).reshape(-1).tolist()
+    B = len(ks)
+    loc = np.full(B * T, -1, dtype=np.int32)
+    bad = 0
+    for b in range(B):
+        fits = 0 <= pl[b] and pl[b] + T <= cap[b]
+        for i in range(T):
+            row = ks[b] + pl[b] + i
+            if fits and 0 <= row < pool.shape[0] and row < 2 ** 31:
+                pool[row, :draft.shape[1]] = draft[b * T + i]
+                loc[b * T + i] = row
+            else:
+                bad += 1
+    return pool, loc, bad
+
+
+def compact_accepted(pool_bits, kv_start, prefix_len, capacity, accept_len, accept_nodes,
+                     T: int, cols: int = D_QK):
+    """Accepted path of request b moved to directly after its prefix.
+
+    With P = prefix_len[b] and n = accept_len[b], the k-th accepted node
+    (accept_nodes[b, k], a draft node whose row is kv_start[b] + P + node)
+    has its first `cols` columns copied to row kv_start[b] + P + k, all n rows
+    read before any is written; then prefix_len[b] becomes P + n.  A request
+    whose n is outside [0, T], whose accepted nodes are outside [0, T), or
+    whose rows fall outside its reserved range (P + T <= capacity[b]) or the
+    pool is left unchanged and counted.  Returns (a copy of the pool, the new
+    prefix_len int32 [B], the number of requests left unchanged)."""
+    pool = np.array(pool_bits, dtype=np.uint16, copy=True, order="C")
+    ks = np.asarray(kv_start).reshape(-1).tolist()
+    pl = np.asarray(prefix_len).reshape(-1).astype(np.int64).tolist()
+    cap = np.asarray(capacity).reshape(-1).tolist()
+    alen = np.asarray(accept_len).reshape(-1).tolist()
+    nodes = np.asarray(accept_nodes).reshape(len(ks), T)
+    new_pl = np.array(pl, dtype=np.int32)
+    bad = 0
+    for b in range(len(ks)):
+        P, n = pl[b], alen[b]
+        path = [int(x) for x in nodes[b, :max(0, min(n, T))]]
+        ok = (0 <= n <= T and 0 <= P and P + T <= cap[b]
+              and ks[b] + P >= 0 and ks[b] + P + T <= pool.shape[0]
+              and all(0 <= x < T for x in path))
+        if not ok:
+            bad += 1
+            continue
+        rows = [pool[ks[b] + P + x, :cols].copy() for x in path]
+        for k, r in enumerate(rows):
+            pool[ks[b] + P + k, :cols] = r
+        new_pl[b] = P + n
+    return pool, new_pl, bad

@@ -715,3 +715,113 @@ def test_pop_slots(oracle_mod):
     assert loc.tolist() == [3, 9, 1, 4] and head == 5
     loc, head = oracle_mod.pop_slots(free, 4, 2, 2)    # the list runs out
     assert loc.tolist() == [4, 8, -1, -1] and head == 8
+
+
+# ---------------------------------------------- contiguous placement and compaction
+
+def _pool(rows, cols=3):
+    """Row r of a small pool holds r*10 + c in column c (easy to read back)."""
+    return (np.arange(rows)[:, None] * 10 + np.arange(cols)[None, :]).astype(np.uint16)
+
+
+def test_append_contiguous_golden(oracle_mod):
+    """Two requests owning rows [0, 6) and [6, 12): prefixes of 2 and 1 rows,
+    three draft nodes each, so request 0's nodes land in rows 2-4 and request
+    1's in rows 7-9 (worked by hand)."""
+    pool = _pool(12)
+    draft = (900 + np.arange(6)[:, None] * 10 + np.arange(2)[None, :]).astype(np.uint16)
+    new, loc, bad = oracle_mod.append_contiguous(pool, draft, [0, 6], [2, 1], [6, 6], 3)
+    assert loc.tolist() == [2, 3, 4, 7, 8, 9] and bad == 0
+    want = pool.copy()
+    for r, row in zip([2, 3, 4, 7, 8, 9], range(6)):
+        want[r, :2] = [900 + row * 10, 901 + row * 10]
+    np.testing.assert_array_equal(new, want)
+
+
+def test_append_contiguous_capacity_and_pool_bounds(oracle_mod):
+    pool = _pool(10)
+    draft = np.ones((6, 3), dtype=np.uint16)
+    # request 0: 4 + 3 > 6 reserved rows; request 1: rows 8, 9, 10 -- the last
+    # outside the pool
+    new, loc, bad = oracle_mod.append_contiguous(pool, draft, [0, 7], [4, 1], [6, 6], 3)
+    assert loc.tolist() == [-1, -1, -1, 8, 9, -1] and bad == 4
+    np.testing.assert_array_equal(new[:8], pool[:8])
+    assert (new[8:10] == 1).all()
+
+
+def test_compact_accepted_golden(oracle_mod):
+    """Continues the append example: request 0 accepts nodes 0 and 2 (rows 2
+    and 4), request 1 accepts node 1 (row 8).  Request 0's rows become
+    2 <- 2, 3 <- 4 and its prefix 2 -> 4; request 1's row 7 <- 8, prefix 1 -> 2
+    (worked by hand)."""
+    pool = _pool(12)
+    new, pl, bad = oracle_mod.compact_accepted(pool, [0, 6], [2, 1], [6, 6], [2, 1],
+                                               [[0, 2, -1], [1, -1, -1]], 3, cols=3)
+    assert pl.tolist() == [4, 2] and bad == 0
+    want = pool.copy()
+    want[3] = pool[4]
+    want[7] = pool[8]
+    np.testing.assert_array_equal(new, want)
+
+
+def test_compact_accepted_reads_before_writing(oracle_mod):
+    """A path in decreasing node order (node 2, then node 0) with P = 1: row
+    1 takes node 2's row (row 3) and row 2 takes node 0's row, which is row 1's
+    old content -- right only when every row is read before any is written."""
+    pool = _pool(8)
+    new, pl, _ = oracle_mod.compact_accepted(pool, [0], [1], [8], [2], [[2, 0, -1]], 3, cols=3)
+    np.testing.assert_array_equal(new[1], pool[3])
+    np.testing.assert_array_equal(new[2], pool[1])
+    assert pl.tolist() == [3]
+
+
+def test_compact_accepted_edge_cases(oracle_mod):
+    pool = _pool(20)
+    # nothing accepted: unchanged pool and prefix; a full chain: identity moves
+    new, pl, bad = oracle_mod.compact_accepted(pool, [0, 10], [3, 2], [8, 8], [0, 4],
+                                               [[-1] * 4, [0, 1, 2, 3]], 4, cols=3)
+    np.testing.assert_array_equal(new, pool)
+    assert pl.tolist() == [3, 6] and bad == 0
+    # a node outside [0, T), an accept count past T, a range past the reserve:
+    # each request left unchanged and counted
+    new, pl, bad = oracle_mod.compact_accepted(pool, [0, 5, 10], [1, 1, 6], [8, 8, 8],
+                                               [1, 5, 1], [[4, -1, -1, -1], [0, 1, 2, 3],
+                                                           [0, -1, -1, -1]], 4, cols=3)
+    np.testing.assert_array_equal(new, pool)
+    assert pl.tolist() == [1, 1, 6] and bad == 3
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_append_then_compact_keeps_the_logical_sequence(oracle_mod, seed):
+    """Invariant: after the append and the compaction, request b's first
+    prefix_len'[b] rows from kv_start[b] are, in order, its prefix rows and then
+    the draft latents of its accepted nodes in path order -- the key sequence a
+    paged step over (prefix slots, accepted nodes' slots) would read next.
+    Written as a gather by list, independently of the in-place moves."""
+    rng = np.random.default_rng(seed)
+    B, T, cols = 3, 5, 4
+    cap = 12
+    ks = np.array([0, cap, 2 * cap]) + 3
+    pl = rng.integers(0, cap - T + 1, size=B)
+    pool = rng.integers(0, 60000, size=(3 * cap + 6, cols)).astype(np.uint16)
+    draft = rng.integers(0, 60000, size=(B * T, cols)).astype(np.uint16)
+    p1, loc, bad = oracle_mod.append_contiguous(pool, draft, ks, pl, [cap] * B, T)
+    assert bad == 0
+    alen = rng.integers(0, T + 1, size=B)
+    nodes = np.full((B, T), -1, dtype=np.int32)
+    for b in range(B):
+        path = np.sort(rng.choice(T, size=alen[b], replace=False))
+        nodes[b, :alen[b]] = path
+    p2, pl2, bad = oracle_mod.compact_accepted(p1, ks, pl, [cap] * B, alen, nodes, T, cols=cols)
+    assert bad == 0 and pl2.tolist() == (pl + alen).tolist()
+    for b in range(B):
+        logical = [p1[ks[b] + j] for j in range(pl[b])] + \
+                  [draft[b * T + int(x)] for x in nodes[b, :alen[b]]]
+        got = [p2[ks[b] + j] for j in range(pl2[b])]
+        for a, g in zip(logical, got):
+            np.testing.assert_array_equal(a, g)
+        # rows outside the request's reserved range are untouched
+    owned = np.zeros(p2.shape[0], dtype=bool)
+    for b in range(B):
+        owned[ks[b]:ks[b] + cap] = True
+    np.testing.assert_array_equal(p2[~owned], pool[~owned])
