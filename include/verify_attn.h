@@ -329,6 +329,64 @@ int verify_attn_defrag(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
                        uint32_t *status, va_stream_t stream);
 
 /*
+ * Contiguous placement of the draft latents, and compaction of the accepted
+ * path: the defragmentation policy the pages name but defer (The Checkpoint
+ * Report, "Input Knowledge Required": defragmentation keeps per-request KV
+ * contiguous; "The Architecture of the Report": the deferred defragmentation
+ * phase).  Read here as: request b owns the pool rows [kv_start[b],
+ * kv_start[b] + kv_capacity[b]); its prefix occupies the first prefix_len[b]
+ * of them; before verify, its T draft latents go to the next T rows (so
+ * verify_attn_contiguous reads prefix and draft keys as one run of rows);
+ * after acceptance, the accepted path's rows move to directly after the
+ * prefix and the prefix grows by the accepted count, so the request stays
+ * contiguous from step to step.
+ *
+ * va_kv_append_contiguous: for every request b and node i < T, writes draft
+ * row b*T + i into the first 576 columns of pool row
+ *   kv_start[b] + prefix_len[b] + i
+ * and sets out_cache_loc[b*T + i] to that row; a node gets no row (-1, row
+ * not written, VA_STATUS_BAD_DST OR-ed into *status) when prefix_len[b] < 0,
+ * prefix_len[b] + T > kv_capacity[b], or the row lies outside [0, num_slots)
+ * or above 2^31 - 1.
+ *   kv_pool        bf16 [num_slots, kv_row_stride] device, 16-byte aligned,
+ *                  kv_row_stride >= 576 and a multiple of 8.
+ *   kv_start       int64 [B] device; prefix_len, kv_capacity int32 [B] device.
+ *   draft_kv       bf16 [B*T, 576] device, contiguous, 16-byte aligned.
+ *   out_cache_loc  int32 [B*T] device or NULL.
+ *   status         uint32 device word or NULL; bits are OR-ed in (the caller
+ *                  clears it).
+ * One warp per draft row; capture-safe, no host sync.  Returns VA_OK or a
+ * VA_ERR_* code before any launch.
+ */
+int va_kv_append_contiguous(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
+                            const int64_t *kv_start, const int32_t *prefix_len,
+                            const int32_t *kv_capacity, const void *draft_kv, int B, int T,
+                            int32_t *out_cache_loc, uint32_t *status, va_stream_t stream);
+
+/*
+ * va_kv_compact_accepted: for every request b, with P = prefix_len[b] and
+ * n = accept_len[b], copies the first 576 columns of row
+ *   kv_start[b] + P + accept_nodes[b*T + k]   to   kv_start[b] + P + k,
+ * k < n, reading all n rows before writing any (a path may list its nodes in
+ * any order), then sets prefix_len[b] = P + n.  accept_len and accept_nodes
+ * are va_tree_accept's outputs.  A request with n outside [0, T], an accepted
+ * node outside [0, T), P < 0, P + T > kv_capacity[b], or rows outside the
+ * pool is left unchanged (pool and prefix_len) and sets VA_STATUS_BAD_DST in
+ * *status (OR-ed in; NULL: not reported).
+ *   accept_len    int32 [B] device; accept_nodes int32 [B, T] device.
+ *   prefix_len    int32 [B] device, read and advanced in place.
+ *   other arguments as for va_kv_append_contiguous.
+ * One CTA per request, the rows staged in shared memory (T * 1152 bytes);
+ * capture-safe, no host sync.  Returns VA_OK or a VA_ERR_* code before any
+ * launch.
+ */
+int va_kv_compact_accepted(void *kv_pool, int64_t num_slots, int64_t kv_row_stride,
+                           const int64_t *kv_start, int32_t *prefix_len,
+                           const int32_t *kv_capacity, const int32_t *accept_len,
+                           const int32_t *accept_nodes, int B, int T, uint32_t *status,
+                           va_stream_t stream);
+
+/*
  * Paged verify attention that allocates nothing and takes no workspace.
  * The pages have no counterpart; this entry point exists for callers that
  * cannot call cudaMalloc: a plugin inside a serving engine whose allocator

@@ -87,6 +87,10 @@ def load() -> ctypes.CDLL:
     lib.va_tree_build.restype = i32
     lib.verify_attn_defrag.argtypes = [P, i64, i64, P, P, P, P, i32, i64, P, P]
     lib.verify_attn_defrag.restype = i32
+    lib.va_kv_append_contiguous.argtypes = [P, i64, i64, P, P, P, P, i32, i32, P, P, P]
+    lib.va_kv_append_contiguous.restype = i32
+    lib.va_kv_compact_accepted.argtypes = [P, i64, i64, P, P, P, P, P, i32, i32, P, P]
+    lib.va_kv_compact_accepted.restype = i32
     lib.verify_attn_paged_noalloc.argtypes = [P, P, i64, i64, P, P, P, P, P, i32, i32, i32, f32,
                                               i32, i32, P, P, P]
     lib.verify_attn_paged_noalloc.restype = i32
@@ -368,6 +372,71 @@ def verify_attn_defrag(kv_pool: torch.Tensor, src_slots: torch.Tensor, src_indpt
         _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(src_slots), _ptr(src_indptr),
         _ptr(dst_base), _ptr(slot_idx_out), B, rows, _ptr(status), _stream(stream))
     _check("verify_attn_defrag", rc)
+
+
+def _placement_args(kv_pool, kv_start, prefix_len, kv_capacity):
+    _dev(kv_pool, "kv_pool", torch.bfloat16)
+    _dev(kv_start, "kv_start", torch.int64)
+    _dev(prefix_len, "prefix_len", torch.int32)
+    _dev(kv_capacity, "kv_capacity", torch.int32)
+    B = kv_start.numel()
+    if prefix_len.numel() != B or kv_capacity.numel() != B:
+        raise ValueError("kv_start, prefix_len and kv_capacity need one entry per request")
+    if kv_pool.dim() != 2 or kv_pool.stride(1) != 1:
+        raise ValueError("kv_pool must be a row-major [num_slots, stride] tensor")
+    return B
+
+
+def kv_append_contiguous(kv_pool: torch.Tensor, kv_start: torch.Tensor, prefix_len: torch.Tensor,
+                         kv_capacity: torch.Tensor, draft_kv: torch.Tensor,
+                         out_cache_loc: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Draft latents of request b (draft_kv rows b*T .. b*T+T-1) into the rows
+    right after its prefix, kv_start[b] + prefix_len[b] + i, within its
+    reserved kv_capacity[b] rows (see va_kv_append_contiguous in
+    verify_attn.h); out_cache_loc (int32 [B*T]) receives the rows."""
+    init(kv_pool.device.index)
+    B = _placement_args(kv_pool, kv_start, prefix_len, kv_capacity)
+    _dev(draft_kv, "draft_kv", torch.bfloat16)
+    if draft_kv.dim() != 2 or draft_kv.shape[1] != D_QK or draft_kv.shape[0] % B != 0 \
+            or not draft_kv.is_contiguous():
+        raise ValueError("draft_kv must be a contiguous [B*T, 576] tensor")
+    T = draft_kv.shape[0] // B
+    if out_cache_loc is not None:
+        _dev(out_cache_loc, "out_cache_loc", torch.int32)
+        if out_cache_loc.numel() != B * T:
+            raise ValueError("out_cache_loc needs B*T entries")
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    rc = load().va_kv_append_contiguous(
+        _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_start), _ptr(prefix_len),
+        _ptr(kv_capacity), _ptr(draft_kv), B, T, _ptr(out_cache_loc), _ptr(status),
+        _stream(stream))
+    _check("va_kv_append_contiguous", rc)
+
+
+def kv_compact_accepted(kv_pool: torch.Tensor, kv_start: torch.Tensor, prefix_len: torch.Tensor,
+                        kv_capacity: torch.Tensor, accept_len: torch.Tensor,
+                        accept_nodes: torch.Tensor, status: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """The accepted path of request b (accept_nodes[b, :accept_len[b]]) moved
+    to the rows right after its prefix, and prefix_len[b] advanced by
+    accept_len[b], in place on the device (see va_kv_compact_accepted in
+    verify_attn.h)."""
+    init(kv_pool.device.index)
+    B = _placement_args(kv_pool, kv_start, prefix_len, kv_capacity)
+    _dev(accept_len, "accept_len", torch.int32)
+    _dev(accept_nodes, "accept_nodes", torch.int32)
+    if accept_len.numel() != B or accept_nodes.numel() % B != 0:
+        raise ValueError("accept_len needs B entries and accept_nodes B*T")
+    T = accept_nodes.numel() // B
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    rc = load().va_kv_compact_accepted(
+        _ptr(kv_pool), kv_pool.shape[0], kv_pool.stride(0), _ptr(kv_start), _ptr(prefix_len),
+        _ptr(kv_capacity), _ptr(accept_len), _ptr(accept_nodes), B, T, _ptr(status),
+        _stream(stream))
+    _check("va_kv_compact_accepted", rc)
 
 
 def tree_accept(root_logits: torch.Tensor, logits: torch.Tensor, draft_tokens: torch.Tensor,

@@ -247,3 +247,42 @@ def test_tree_build_rejects_bad_arguments_before_any_launch(lib):
     assert _tree(lib, K=1, D=4, T=5) == -2
     assert _tree(lib, lp=A16 + 2) == -3
     assert _tree(lib, loc=A16 + 1) == -3
+
+
+def _append(lib, **over):
+    a = dict(pool=A16, num_slots=4096, stride=576, start=A16, prefix=A16, cap=A16, draft=A16,
+             B=2, T=4, loc=A16, status=None)
+    a.update(over)
+    return lib.va_kv_append_contiguous(a["pool"], a["num_slots"], a["stride"], a["start"],
+                                       a["prefix"], a["cap"], a["draft"], a["B"], a["T"],
+                                       a["loc"], a["status"], None)
+
+
+def _compact(lib, **over):
+    a = dict(pool=A16, num_slots=4096, stride=576, start=A16, prefix=A16, cap=A16, alen=A16,
+             nodes=A16, B=2, T=4, status=None)
+    a.update(over)
+    return lib.va_kv_compact_accepted(a["pool"], a["num_slots"], a["stride"], a["start"],
+                                      a["prefix"], a["cap"], a["alen"], a["nodes"], a["B"], a["T"],
+                                      a["status"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(pool=None), -1), (dict(start=None), -1), (dict(prefix=None), -1), (dict(cap=None), -1),
+    (dict(draft=None), -1),
+    (dict(B=0), -2), (dict(T=0), -2), (dict(T=65), -2), (dict(num_slots=0), -2),
+    (dict(stride=512), -2),
+    (dict(stride=580), -3), (dict(pool=A16 + 8), -3), (dict(start=A16 + 4), -3),
+    (dict(draft=A16 + 8), -3), (dict(loc=A16 + 2), -3),
+])
+def test_append_contiguous_argument_errors(lib, over, code):
+    assert _append(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(pool=None), -1), (dict(alen=None), -1), (dict(nodes=None), -1), (dict(cap=None), -1),
+    (dict(B=0), -2), (dict(T=65), -2), (dict(stride=100), -2),
+    (dict(pool=A16 + 2), -3), (dict(alen=A16 + 2), -3), (dict(prefix=A16 + 1), -3),
+])
+def test_compact_accepted_argument_errors(lib, over, code):
+    assert _compact(lib, **over) == code
