@@ -852,6 +852,93 @@ def bench_defrag(va, pool, dev, hbm_peak) -> dict:
             "frac_hbm": moved / (d_us * 1e-6) / 1e9 / hbm_peak}
 
 
+def bench_contiguous_decode(va, dev, tc_peak) -> dict:
+    """The headline workload's shapes (8 requests, H=64, T=16, the same
+    prefixes) kept contiguous by the placement policy: each request owns a
+    reserved range of rows; one decode step is the draft rows placed after the
+    prefix, the contiguous verify and the compaction of a 3-node accepted path
+    (the prefix lengths are restored at the start of every step, so every step
+    is the same).  Timed as one-step CUDA graphs (events), beside the
+    contiguous verify alone; the KV (266 MB) is larger than L2."""
+    hs = synth.spec(HEADLINE)
+    B, H, T = hs.B, hs.H, hs.T
+    prefix = np.array(hs.prefix, dtype=np.int32)
+    cap = prefix + 64
+    starts = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int64)
+    pool = device_pool(int(cap.sum()), seed=11, dev=dev)
+    g = torch.Generator(device=dev).manual_seed(12)
+    q = torch.randn(B * T, H, synth.D_QK, generator=g, device=dev).to(torch.bfloat16)
+    draft = torch.randn(B * T, synth.D_QK, generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(13)
+    par = np.full((B, T), -1, dtype=np.int32)
+    for i in range(1, T):
+        par[:, i] = rng.integers(-1, i, size=B)
+    par[:, 1] = 0
+    par[:, 2] = 1                                  # nodes 0 -> 1 -> 2 form the accepted path
+    d_par = torch.from_numpy(par).to(dev)
+    d_start = torch.from_numpy(starts).to(dev)
+    d_cap = torch.from_numpy(cap).to(dev)
+    pl0 = torch.from_numpy(prefix).to(dev)
+    d_pl = pl0.clone()
+    alen = torch.full((B,), 3, dtype=torch.int32, device=dev)
+    nodes = torch.full((B, T), -1, dtype=torch.int32, device=dev)
+    nodes[:, :3] = torch.arange(3, dtype=torch.int32, device=dev)
+    loc = torch.empty(B * T, dtype=torch.int32, device=dev)
+    ws, ns = va.alloc_workspace(B, T, H, 0, va.PATH_AUTO, dev)
+    out = torch.empty(B * T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B * T, H, dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+
+    def step(full: bool):
+        d_pl.copy_(pl0)
+        if full:
+            va.kv_append_contiguous(pool, d_start, d_pl, d_cap, draft, loc, stream=st)
+        va.verify_attn_contiguous(q, pool, d_start, d_pl, d_par, sm_scale=synth.SM_SCALE,
+                                  nsplit=ns, workspace=ws, out=out, lse=lse, stream=st)
+        if full:
+            va.kv_compact_accepted(pool, d_start, d_pl, d_cap, alen, nodes, stream=st)
+
+    res = {}
+    for name, full in (("decode_step", True), ("verify_only", False)):
+        st.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            step(full)                              # warm-up outside the capture
+        st.synchronize()
+        with torch.cuda.graph(graph, stream=st):
+            step(full)
+        for _ in range(5):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps * 1e3
+        del graph
+    # algorithmic flops of the verify: every prefix key and each node's
+    # ancestors-or-self among the draft keys, for every row
+    depth_set = np.zeros((B, T), dtype=np.int64)
+    for b in range(B):
+        for i in range(T):
+            n, j = 1, par[b, i]
+            while j >= 0:
+                n, j = n + 1, par[b, j]
+            depth_set[b, i] = n
+    pairs = float(sum((prefix[b] * T + depth_set[b].sum()) * H for b in range(B)))
+    flops = 2176.0 * pairs
+    kv_bytes = float((prefix + T).sum()) * 1152
+    return {"us_per_step": res["decode_step"], "verify_only_us": res["verify_only"],
+            "placement_and_compaction_us": res["decode_step"] - res["verify_only"],
+            "gbs": kv_bytes / (res["decode_step"] * 1e-6) / 1e9,
+            "tflops": flops / (res["decode_step"] * 1e-6) / 1e12,
+            "frac_tensor": flops / (res["decode_step"] * 1e-6) / 1e12 / tc_peak,
+            "nsplit": ns, "timing": "one-step CUDA graphs, events; prefix lengths restored each step"}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -969,6 +1056,10 @@ def main():
             bench_tree_build(va, dev)
         configs["defrag 65536 scattered rows -> contiguous"] = bench_defrag(va, pool, dev,
                                                                             hbm_peak)
+        configs["contiguous decode step, batched H=64 T=16 (placement + contiguous verify + "
+                "compaction; the same requests as the headline, kept contiguous)"] = \
+            bench_contiguous_decode(va, dev, tc_peak)
+        torch.cuda.empty_cache()
 
     cpu, parity = (None, None)
     if rank == 0 and not args.no_cpu:
