@@ -69,6 +69,8 @@ __device__ __forceinline__ int key_rank(uint64_t key, int d) {
 __global__ void __launch_bounds__(kTreeWarps * 32) tree_build_kernel(TreeParams p) {
   __shared__ float s_lp[kTreeWarps][kMaxDepth][kMaxCand];     // ranked log-probabilities
   __shared__ int32_t s_tok[kTreeWarps][kMaxDepth][kMaxCand];  // ranked tokens
+  __shared__ float s_rlp[kTreeWarps][kMaxDepth * kMaxCand];   // as drafted
+  __shared__ int32_t s_rtok[kTreeWarps][kMaxDepth * kMaxCand];
   __shared__ int64_t s_head;
   __shared__ uint32_t s_flags;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,15 +81,40 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_build_kernel(TreeParams 
   __syncthreads();
   const int64_t head = s_head;
   for (int b = warp; b < p.B; b += kTreeWarps) {
-    // 1. rank each depth's candidates: lane k < K finds how many candidates
-    // beat its own and stores itself at that rank
+    // 1. the request's D*K candidates, all loads in flight at once (one
+    // memory round trip, not one per depth), then each depth ranked: lane
+    // k < K finds how many candidates beat its own and stores itself at that
+    // rank
+    {
+      constexpr int kLoads = (kMaxDepth * kMaxCand + 31) / 32;
+      const int dk = p.D * p.K;
+      const size_t base = size_t(b) * dk;
+      float lv[kLoads];
+      int32_t lt[kLoads];
+#pragma unroll
+      for (int j = 0; j < kLoads; ++j) {
+        const int e = lane + 32 * j;
+        if (e < dk) {
+          lv[j] = p.cand_logp[base + e];
+          lt[j] = p.cand_tokens[base + e];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kLoads; ++j) {
+        const int e = lane + 32 * j;
+        if (e < dk) {
+          s_rlp[warp][e] = lv[j];
+          s_rtok[warp][e] = lt[j];
+        }
+      }
+      __syncwarp();
+    }
     for (int d = 0; d < p.D; ++d) {
-      const size_t base = (size_t(b) * p.D + d) * p.K;
       float v = -INFINITY;
       int32_t tk = 0;
       if (lane < p.K) {
-        v = p.cand_logp[base + lane];
-        tk = p.cand_tokens[base + lane];
+        v = s_rlp[warp][d * p.K + lane];
+        tk = s_rtok[warp][d * p.K + lane];
         if (!(v < INFINITY)) v = -INFINITY;    // NaN, +inf
       }
       int rank = 0;
