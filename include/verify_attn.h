@@ -141,7 +141,8 @@ size_t va_workspace_bytes(int B, int T, int H, int nsplit);
  *                 non-NULL it is used and tree_parent is ignored.
  *   B, T, H       1 <= B, 1 <= T <= 64, 1 <= H.
  *   sm_scale      scale applied to the 576-wide dot product.
- *   nsplit        key-range splits per (request, row block); 0 = automatic
+ *   nsplit        key-range splits per (request, row unit: 128 rows, or 256
+ *                 with two-SM products); 0 = automatic
  *                 (The Commit That Locked In 6x Decode, "2. NSPLIT=64 for TP8
  *                 Occupancy").  Splits that would hold fewer than 64 keys are
  *                 dropped on the device from the actual prefix length.
