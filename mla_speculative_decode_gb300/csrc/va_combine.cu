@@ -79,12 +79,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int b = row / p.rows_per_req;
   constexpr int kWarps = kCombineThreads / 32;
   // The request's split count comes from its bounds, which are inputs of the
-  // call rather than results of the split-K kernel (that kernel began after
-  // the stream's earlier work had completed), so they are read before the
-  // wait; only the splits that ran are loaded below.
+  // call rather than results of the split-K kernel (this kernel is scheduled
+  // only once every split-K CTA has passed its own wait for the stream's
+  // earlier work), so they are read before the wait; only the splits that ran
+  // are loaded below.
   const ReqInfo ri = req_info(p, b, false);
   const int ne = split_range(ri.N, p.nsplit, 0).nsplit_eff;
   griddep_wait();   // the split-K kernel's partials are complete and visible
+  // the stream's next kernel, when launched as a programmatic dependent (the
+  // next call's split-K kernel), may start its set-up now; it waits for
+  // this kernel's completion before reading anything
+  griddep_launch_dependents();
   const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + chunk * kCombineCols + lane * 4;
   const size_t sstride = size_t(rows_total) * kDv;
 
@@ -212,6 +217,10 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_rows_kernel(Params p) 
   // results of the split-K kernel), before the wait
   const int ne = live ? split_range(req_info(p, b, false).N, p.nsplit, 0).nsplit_eff : 0;
   griddep_wait();   // the split-K kernel's partials are complete and visible
+  // the stream's next kernel, when launched as a programmatic dependent (the
+  // next call's split-K kernel), may start its set-up now; it waits for
+  // this kernel's completion before reading anything
+  griddep_launch_dependents();
   if (live) {
     const size_t col = size_t(chunk) * (32 * kVec) + size_t(lane) * kVec;
     const __nv_bfloat16* po = p.part_o + size_t(row) * kDv + col;

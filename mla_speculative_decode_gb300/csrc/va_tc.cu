@@ -556,13 +556,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  griddep_launch_dependents();   // the merge kernel may be scheduled as clusters retire
   // The kernel computes its rows' ancestor masks itself and keeps its status
   // bits in shared memory, stored to its own workspace word at the end; the
   // merge kernel ORs those into the status word.  It is the call's first
-  // kernel, except when the call appends draft rows first: then the kernel
-  // before it writes them, and the producers wait (griddepcontrol.wait)
-  // before a tile holding draft keys.
+  // kernel, launched as a programmatic dependent of the stream's previous
+  // kernel: its clusters may be resident while that kernel finishes, and
+  // wait here, before reading any input, until it has completed.  When the
+  // call appends draft rows first, the append kernel (launched after the
+  // stream's earlier work) precedes it instead, and the producers wait
+  // (griddepcontrol.wait) only before a tile holding draft keys.
+  if (!p.draft_kv) griddep_wait();
+  // the merge kernel may be scheduled as clusters retire (only after the
+  // wait above: it reads the call's bounds before its own wait)
+  griddep_launch_dependents();
   const ReqInfo ri = req_info(p, b, false);
   const SplitRange sr = split_range(ri.N, p.nsplit, split);
   // this CTA's status word, for the merge kernel to OR into the status word
@@ -1388,9 +1394,11 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
         encode_pool_map(&tv, p, pair ? 2 : kVBlocks, kTile))
       box3d = 1;
   }
-  // After the draft-row append kernel the clusters may start while it runs
-  // (programmatic stream serialization; see the producers' griddepcontrol.wait);
-  // as the call's first kernel, a plain launch after the stream's earlier work.
+  // A programmatic dependent of the stream's previous kernel (programmatic
+  // stream serialization): after the draft-row append kernel the clusters
+  // run while it does (see the producers' griddepcontrol.wait); as the call's
+  // first kernel they may start while the stream's previous kernel finishes
+  // and wait for it before reading any input.
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(unsigned(ctas * p.nsplit), unsigned(ceil_div(p.rows_per_req, unit)),
@@ -1406,7 +1414,7 @@ cudaError_t launch_partial_tc(const Params& p, int /*num_sms*/, cudaStream_t st)
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.draft_kv ? 2 : 1;
+  cfg.numAttrs = 2;
   return pair ? cudaLaunchKernelEx(&cfg, partial_tc_kernel<true>, p, tk, tv, t2, tq, box3d)
               : cudaLaunchKernelEx(&cfg, partial_tc_kernel<false>, p, tk, tv, t2, tq, box3d);
 }
