@@ -26,6 +26,14 @@
  *    by the caller).
  *  - Step-varying data (prefix lengths, slot tables, tree parents) is read on
  *    the device, so one captured graph replays across decode steps.
+ *  - Stream order holds as for any launch.  The attention calls' first kernel
+ *    is a programmatic dependent of the stream's previous kernel: its CTAs
+ *    may become resident while that kernel finishes, but read no input until
+ *    it has completed (griddepcontrol.wait).  Their last kernel lets the
+ *    stream's next kernel do the same once it has itself passed that point,
+ *    so a caller's next kernel launched as a programmatic dependent must wait
+ *    (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads the
+ *    call's outputs; a plainly launched one is ordered as usual.
  *  - Host-checkable argument errors return a negative VA_ERR_* code before any
  *    device work is enqueued.  Device-data errors (a slot outside the pool, a
  *    parent that is not an earlier node, a slot list shorter than
