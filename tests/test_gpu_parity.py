@@ -348,6 +348,65 @@ def test_graph_capture_replay_with_new_inputs(va, path):
     assert va.read_status(ws) == 0
 
 
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_inputs_written_by_the_previous_kernel(va, path, graph):
+    """The call's first kernel may start while the stream's previous kernel
+    finishes (programmatic dependent launch) but must read no input before it
+    has completed: the step's q, slots, parents and prefix lengths are written
+    by device kernels (elementwise multiplies by 1, prefix lengths last)
+    immediately before the call, after a call on the old contents."""
+    s1 = synth.Spec("pdl", B=2, H=8, T=16, prefix=[3000, 1500], num_slots=1 << 15, seed=43)
+    _need(va, path, s1.B, s1.T, s1.H)
+    w1 = synth.make(s1)
+    w2 = synth.make(synth.Spec("pdl", B=2, H=8, T=16, prefix=[2500, 2900], num_slots=1 << 15,
+                               seed=44))
+    w2.kv_pool = w1.kv_pool
+    d = _gpu.to_device(w1)
+    cap = max(w1.slot_idx.numel(), w2.slot_idx.numel())
+    slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    slots[:w1.slot_idx.numel()] = d["slot_idx"]
+    d["slot_idx"] = slots
+    src = {"q": w2.q.cuda(), "kv_indptr": w2.kv_indptr.cuda(), "parents": w2.parents.cuda(),
+           "prefix_len": w2.prefix_len.cuda()}
+    src_slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    src_slots[:w2.slot_idx.numel()] = w2.slot_idx.cuda()
+    ws, ns = va.alloc_workspace(s1.B, s1.T, s1.H, 0, path)
+    out = torch.empty(s1.B * s1.T, s1.H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(s1.B * s1.T, s1.H, dtype=torch.float32, device="cuda")
+
+    def step():
+        _gpu.run(va, d, w1, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
+        torch.mul(src["q"], 1, out=d["q"])
+        torch.mul(src_slots, 1, out=d["slot_idx"])
+        torch.mul(src["kv_indptr"], 1, out=d["kv_indptr"])
+        torch.mul(src["parents"], 1, out=d["parents"])
+        torch.mul(src["prefix_len"], 1, out=d["prefix_len"])
+        _gpu.run(va, d, w2, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        if graph:
+            step()   # warm-up on the side stream before capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            # the old contents again, then one replay
+            for k in ("q", "kv_indptr", "parents", "prefix_len"):
+                d[k].copy_(getattr(w1, k).cuda())
+            d["slot_idx"][:w1.slot_idx.numel()].copy_(w1.slot_idx.cuda())
+            out.fill_(float("nan"))
+            g.replay()
+        else:
+            step()
+    torch.cuda.synchronize()
+    ref_o, ref_l = _gpu.reference(w2)
+    _gpu.compare(out, lse, ref_o, ref_l)
+    assert va.read_status(ws) == 0
+
+
 def test_deterministic(va):
     w = synth.make(synth.spec("tp8"))
     d = _gpu.to_device(w)
