@@ -350,12 +350,14 @@ def test_graph_capture_replay_with_new_inputs(va, path):
 
 @pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
 @pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
-def test_inputs_written_by_the_previous_kernel(va, path, graph):
+@pytest.mark.parametrize("writer", ["kernel", "copy"])
+def test_inputs_written_by_the_previous_kernel(va, path, graph, writer):
     """The call's first kernel may start while the stream's previous kernel
     finishes (programmatic dependent launch) but must read no input before it
     has completed: the step's q, slots, parents and prefix lengths are written
-    by device kernels (elementwise multiplies by 1, prefix lengths last)
-    immediately before the call, after a call on the old contents."""
+    immediately before the call (prefix lengths last), after a call on the old
+    contents -- by device kernels (elementwise multiplies by 1) or by copies
+    from pinned host memory."""
     s1 = synth.Spec("pdl", B=2, H=8, T=16, prefix=[3000, 1500], num_slots=1 << 15, seed=43)
     _need(va, path, s1.B, s1.T, s1.H)
     w1 = synth.make(s1)
@@ -367,21 +369,31 @@ def test_inputs_written_by_the_previous_kernel(va, path, graph):
     slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
     slots[:w1.slot_idx.numel()] = d["slot_idx"]
     d["slot_idx"] = slots
-    src = {"q": w2.q.cuda(), "kv_indptr": w2.kv_indptr.cuda(), "parents": w2.parents.cuda(),
-           "prefix_len": w2.prefix_len.cuda()}
-    src_slots = torch.zeros(cap, dtype=torch.int32, device="cuda")
-    src_slots[:w2.slot_idx.numel()] = w2.slot_idx.cuda()
+    on = "cuda" if writer == "kernel" else "cpu"
+    src = {"q": w2.q.to(on), "kv_indptr": w2.kv_indptr.to(on), "parents": w2.parents.to(on),
+           "prefix_len": w2.prefix_len.to(on)}
+    src_slots = torch.zeros(cap, dtype=torch.int32, device=on)
+    src_slots[:w2.slot_idx.numel()] = w2.slot_idx
+    if writer == "copy":
+        src = {k: v.pin_memory() for k, v in src.items()}
+        src_slots = src_slots.pin_memory()
+
+    def write(dst, val):
+        if writer == "kernel":
+            torch.mul(val, 1, out=dst)
+        else:
+            dst.copy_(val, non_blocking=True)
     ws, ns = va.alloc_workspace(s1.B, s1.T, s1.H, 0, path)
     out = torch.empty(s1.B * s1.T, s1.H, 512, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(s1.B * s1.T, s1.H, dtype=torch.float32, device="cuda")
 
     def step():
         _gpu.run(va, d, w1, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
-        torch.mul(src["q"], 1, out=d["q"])
-        torch.mul(src_slots, 1, out=d["slot_idx"])
-        torch.mul(src["kv_indptr"], 1, out=d["kv_indptr"])
-        torch.mul(src["parents"], 1, out=d["parents"])
-        torch.mul(src["prefix_len"], 1, out=d["prefix_len"])
+        write(d["q"], src["q"])
+        write(d["slot_idx"], src_slots)
+        write(d["kv_indptr"], src["kv_indptr"])
+        write(d["parents"], src["parents"])
+        write(d["prefix_len"], src["prefix_len"])
         _gpu.run(va, d, w2, path=path, nsplit=ns, workspace=ws, out=out, lse=lse)
 
     stream = torch.cuda.Stream()
