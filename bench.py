@@ -349,6 +349,11 @@ class Step:
 
 
 STEPS_PER_GRAPH = 8
+# The end-to-end leg's graphs hold more steps: each graph joins its copy
+# streams at the end, so the first upload of the next graph cannot overlap
+# the last kernels of this one (on the batched step 553.5 us per step end to
+# end with 8 steps per graph, 543.9 with 40).
+E2E_STEPS_PER_GRAPH = 40
 
 
 def capture_graphs(step: Step, K: int, with_events: bool = False):
@@ -615,8 +620,9 @@ def e2e_leg(va, step: Step, K: int, W: int, dist, dev):
     one device-to-host copy into pinned memory.  Two input and two result
     buffers alternate, and the copies run on their own streams, so step k+1's
     upload and step k-1's read-back overlap step k's kernels.  Steps are
-    captured eight to a CUDA graph (streams forked and joined inside the
-    capture) and replayed; exactly K steps are timed."""
+    captured E2E_STEPS_PER_GRAPH to a CUDA graph (streams forked and joined
+    inside the capture; a last graph holds the remainder) and replayed;
+    exactly K steps are timed."""
     def align(n):
         return (n + 255) // 256 * 256
 
@@ -709,7 +715,7 @@ def e2e_leg(va, step: Step, K: int, W: int, dist, dev):
     dlse0 = ref0[l_off:res_bytes].view(step.lse.dtype).view(step.lse.shape)
     assert torch.equal(dout0, step.out) and torch.equal(dlse0, step.lse), "e2e path differs"
     assert torch.equal(hress[0], ref0.cpu()), "e2e read-back differs"
-    per = STEPS_PER_GRAPH
+    per = E2E_STEPS_PER_GRAPH
     graphs = []
     for gi in range(max(1, min(4, len(hins) // per))):
         g = torch.cuda.CUDAGraph()
@@ -748,7 +754,8 @@ def e2e_leg(va, step: Step, K: int, W: int, dist, dev):
                     "copy), the verify call (prepared once with va.prepare_paged) launched, out "
                     "and lse read back (one D2H copy); two buffer sets alternate so that the "
                     "copies of neighbouring steps overlap a step's kernels on separate streams; "
-                    "steps captured eight to a CUDA graph and replayed"}
+                    f"steps captured {E2E_STEPS_PER_GRAPH} to a CUDA graph (the remainder in one "
+                    "more) and replayed"}
 
 
 # ------------------------------------------------------------------ main
