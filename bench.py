@@ -348,19 +348,23 @@ class Step:
                                   out=self.out, lse=self.lse, stream=stream)
 
 
-STEPS_PER_GRAPH = 8
-# The end-to-end leg's graphs hold more steps: each graph joins its copy
-# streams at the end, so the first upload of the next graph cannot overlap
-# the last kernels of this one (on the batched step 553.5 us per step end to
-# end with 8 steps per graph, 543.9 with 40).
-E2E_STEPS_PER_GRAPH = 40
+# Steps per CUDA graph.  A graph boundary costs the overlap of consecutive
+# steps (the next step's split-K kernel cannot start while this graph's last
+# merge runs; in the end-to-end leg each graph also joins its copy streams, so
+# the next graph's first upload cannot overlap this graph's last kernels).
+# Measured with 8 and 40 steps per graph: TP8 slice 15.64 -> 15.33 us, H=8
+# P=16384 contiguous 18.53 -> 18.17 us, batched step unchanged (535.5 us),
+# batched end to end 553.5 -> 543.9 us.
+STEPS_PER_GRAPH = 40
+E2E_STEPS_PER_GRAPH = STEPS_PER_GRAPH
 
 
 def capture_graphs(step: Step, K: int, with_events: bool = False):
     """CUDA graphs over the rotated slot tables: graphs of STEPS_PER_GRAPH
     consecutive steps (each on its own table), as a serving loop would capture
-    them, and -- when K is not a multiple of that -- one graph of the K % 8
-    remaining steps, so that exactly K steps can be replayed.  With events:
+    them, and -- when K is not a multiple of that -- one graph of the
+    K % STEPS_PER_GRAPH remaining steps, so that exactly K steps can be
+    replayed.  With events:
     one-step graphs with event records around the split-K kernel instead."""
     va = step.va
     s = torch.cuda.Stream()
@@ -401,7 +405,7 @@ def capture_graphs(step: Step, K: int, with_events: bool = False):
 
 
 def replay_steps(graphs, K: int):
-    """Replays exactly K steps: K // 8 eight-step graphs, then the tail graph."""
+    """Replays exactly K steps: K // STEPS_PER_GRAPH full graphs, then the tail graph."""
     full, tail = graphs
     for r in range(K // STEPS_PER_GRAPH):
         full[r % len(full)].replay()
@@ -1085,8 +1089,9 @@ def main():
                           f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
                        launch=f"CUDA graphs of {STEPS_PER_GRAPH} steps (plus one graph of the "
                               f"{args.steps % STEPS_PER_GRAPH} remaining steps when --steps is "
-                              "not a multiple of 8): exactly --steps steps timed; programmatic "
-                              "dependent launch between the kernels of a step",
+                              f"not a multiple of {STEPS_PER_GRAPH}): exactly --steps steps "
+                              "timed; programmatic dependent launch between the kernels of a "
+                              "step and between steps",
                        parallelism=f"replicas x{world}"),
         "headline": head,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
