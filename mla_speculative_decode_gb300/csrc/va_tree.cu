@@ -61,6 +61,14 @@ __device__ __forceinline__ bool better(float sa, uint64_t ka, float sb, uint64_t
   return sa > sb || (sa == sb && ka < kb);
 }
 
+// Unsigned key with the order of the scores (which are never NaN: the
+// candidates' NaN and +inf count as -inf); -0 counts as +0, as it compares
+// equal to it.  Every score maps above 0.
+__device__ __forceinline__ uint32_t score_order(float sc) {
+  const uint32_t u = __float_as_uint(sc == 0.f ? 0.f : sc);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ int key_depth(uint64_t key) { return int(key >> 60); }
 __device__ __forceinline__ int key_rank(uint64_t key, int d) {
   return int((key >> (56 - 4 * d)) & 15u);
@@ -162,16 +170,23 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_build_kernel(TreeParams 
         }
       }
       int be = bj < 0 ? -1 : bj * 32 + lane;   // frontier index of the lane's best
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        const uint64_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe >= 0 && (be < 0 || better(os, ok, bs, bk))) {
-          bs = os;
-          bk = ok;
-          be = oe;
-        }
+      // The warp's best with three reductions instead of a shuffle tree: the
+      // highest score (as an order-preserving unsigned key; a lane without an
+      // entry offers 0, below every score), then among the lanes holding it
+      // the smallest node key, high word then low word.  Node keys are
+      // unique, so exactly one lane wins.
+      {
+        const uint32_t sk = be < 0 ? 0u : score_order(bs);
+        const uint32_t smax = __reduce_max_sync(0xffffffffu, sk);
+        const bool top = be >= 0 && sk == smax;
+        const uint32_t hi = uint32_t(bk >> 32), lo = uint32_t(bk);
+        const uint32_t hmin = __reduce_min_sync(0xffffffffu, top ? hi : 0xffffffffu);
+        const bool top2 = top && hi == hmin;
+        const uint32_t lmin = __reduce_min_sync(0xffffffffu, top2 ? lo : 0xffffffffu);
+        const int src = __ffs(__ballot_sync(0xffffffffu, top2 && lo == lmin)) - 1;
+        bs = __shfl_sync(0xffffffffu, bs, src);
+        bk = (uint64_t(hmin) << 32) | lmin;
+        be = __shfl_sync(0xffffffffu, be, src);
       }
       // the winner's parent fields, from the lane that holds it
       const int wl = be & 31, wj = be >> 5;
