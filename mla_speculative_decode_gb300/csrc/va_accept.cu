@@ -15,7 +15,8 @@
 //    each writing its best (value, index) to the workspace.  Every logit is
 //    read once: HBM-bound.
 //  - accept_walk_kernel: one warp per request merges its rows' chunks (a
-//    lane per row) and walks the tree.
+//    lane per row) and walks the tree, a vote of the lanes per step (lane
+//    c % 32 holding node c's parent, token and slot).
 // The argmax is the lowest index among the largest non-NaN values (0 for a
 // row of NaN only); both kernels compare with the same rule, so the result
 // does not depend on the chunking.
@@ -148,38 +149,57 @@ __global__ void __launch_bounds__(kWalkWarps * 32) accept_walk_kernel(AcceptPara
     tok[warp][k] = bi < a.V ? bi : 0;   // a row of NaN only: token 0
   }
   __syncwarp();
-  if (lane != 0) return;
+  // Node c = lane + 32h (h = 0, 1; T <= 64) in registers of lane c % 32: its
+  // parent (one that is not an earlier node counts as the prefix, and is
+  // flagged), its draft token and its slot; -2 marks "no node".
   const int32_t* par = a.parent + size_t(b) * T;
   const int32_t* tk = a.tokens + size_t(b) * T;
+  const int32_t* sl = a.slots ? a.slots + size_t(b) * T : nullptr;
+  int pc[2], tc[2], sc[2];
   bool bad = false;
-  for (int c = 0; c < T; ++c) bad |= par[c] < -1 || par[c] >= c;
-  // Each accepted node is a child of the previous one, so has a larger index
-  // (a node whose parent is not an earlier node counts as a child of the
-  // prefix): at most T steps.
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    pc[h] = -2;
+    tc[h] = 0;
+    sc[h] = -1;
+    if (c < T) {
+      const int q = par[c];
+      const bool ok = q >= -1 && q < c;
+      bad |= !ok;
+      pc[h] = ok ? q : -1;
+      tc[h] = tk[c];
+      if (sl) sc[h] = sl[c];
+    }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  // Each accepted node is a child of the previous one, so has a larger index:
+  // at most T steps, each one vote of the lanes (the lowest-numbered child of
+  // `cur` whose draft token is the target's token `t`).
   int cur = -1, n = 0, t = tok[warp][0];
   for (;;) {
-    int pick = -1;
-    for (int c = cur + 1; c < T; ++c) {
-      const int pc = (par[c] < -1 || par[c] >= c) ? -1 : par[c];
-      if (pc == cur && tk[c] == t) {
-        pick = c;
-        break;
-      }
-    }
+    const uint32_t m0 = __ballot_sync(0xffffffffu, lane > cur && pc[0] == cur && tc[0] == t);
+    const uint32_t m1 = __ballot_sync(0xffffffffu, lane + 32 > cur && pc[1] == cur && tc[1] == t);
+    const int pick = m0 ? __ffs(m0) - 1 : (m1 ? 32 + __ffs(m1) - 1 : -1);
     if (pick < 0) break;
-    a.accept_nodes[size_t(b) * T + n] = pick;
-    if (a.accept_slots) a.accept_slots[size_t(b) * T + n] = a.slots ? a.slots[size_t(b) * T + pick] : -1;
+    const int ps = __shfl_sync(0xffffffffu, pick < 32 ? sc[0] : sc[1], pick & 31);
+    if (lane == 0) {
+      a.accept_nodes[size_t(b) * T + n] = pick;
+      if (a.accept_slots) a.accept_slots[size_t(b) * T + n] = ps;
+    }
     ++n;
     cur = pick;
     t = tok[warp][pick + 1];
   }
-  for (int m = n; m < T; ++m) {
+  for (int m = n + lane; m < T; m += 32) {
     a.accept_nodes[size_t(b) * T + m] = -1;
     if (a.accept_slots) a.accept_slots[size_t(b) * T + m] = -1;
   }
-  a.accept_len[b] = n;
-  a.bonus[b] = t;
-  if (bad) atomicOr(a.status, VA_STATUS_BAD_PARENT);
+  if (lane == 0) {
+    a.accept_len[b] = n;
+    a.bonus[b] = t;
+    if (bad) atomicOr(a.status, VA_STATUS_BAD_PARENT);
+  }
 }
 
 struct AcceptLayout {
