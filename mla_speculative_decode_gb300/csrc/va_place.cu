@@ -51,6 +51,8 @@ __device__ __forceinline__ int64_t draft_row(const PlaceParams& p, int b, int i)
 // One warp per draft row: row b*T + i of the draft latents into the first
 // 576 columns of the request's row kv_start[b] + prefix_len[b] + i.
 __global__ void __launch_bounds__(kPlaceWarps * 32) append_contiguous_kernel(PlaceParams p) {
+  griddep_wait();                // the stream's previous kernel has completed
+  griddep_launch_dependents();   // the next kernel may start its set-up
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * kPlaceWarps + (threadIdx.x >> 5);
   if (r >= p.B * p.T) return;
@@ -70,31 +72,32 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) append_contiguous_kernel(Pla
 // moves to kv_start + P + k, every row read into shared memory before any is
 // written (a path may list its nodes in any order), then prefix_len += n.  A
 // request whose accept count, nodes or rows are out of range is left as it is
-// and flagged.
+// and flagged.  Thread k checks node k, all at once.
 __global__ void __launch_bounds__(kPlaceWarps * 32) compact_accepted_kernel(PlaceParams p) {
   extern __shared__ __align__(16) uint4 stage[];   // [T][72]
-  __shared__ int s_ok;
+  __shared__ int s_node[VA_T_MAX];
+  griddep_wait();                // the stream's previous kernel has completed
+  griddep_launch_dependents();   // the next kernel may start its set-up
   const int b = blockIdx.x, tid = threadIdx.x;
   const int T = p.T;
   const int n = p.accept_len[b];
   const int64_t P = p.prefix_len[b];
   const int64_t base = p.kv_start[b] + P;
-  if (tid == 0) {
-    bool ok = n >= 0 && n <= T && P >= 0 && P + T <= int64_t(p.capacity[b]) && base >= 0 &&
-              base + T <= p.num_slots;
-    for (int k = 0; ok && k < n; ++k) {
-      const int node = p.accept_nodes[size_t(b) * T + k];
-      ok = node >= 0 && node < T;
-    }
-    s_ok = ok ? 1 : 0;
-    if (!ok && p.status) atomicOr(p.status, VA_STATUS_BAD_DST);
+  const bool req_ok = n >= 0 && n <= T && P >= 0 && P + T <= int64_t(p.capacity[b]) &&
+                      base >= 0 && base + T <= p.num_slots;
+  bool ok = true;
+  if (req_ok && tid < n) {
+    const int node = p.accept_nodes[size_t(b) * T + tid];
+    ok = node >= 0 && node < T;
+    s_node[tid] = node;
   }
-  __syncthreads();
-  if (!s_ok) return;
+  if (!__syncthreads_and(req_ok && ok)) {
+    if (tid == 0 && p.status) atomicOr(p.status, VA_STATUS_BAD_DST);
+    return;
+  }
   for (int e = tid; e < n * kRowChunks; e += blockDim.x) {
     const int k = e / kRowChunks, c = e - k * kRowChunks;
-    const int node = p.accept_nodes[size_t(b) * T + k];
-    stage[e] = reinterpret_cast<const uint4*>(p.pool + (base + node) * p.stride)[c];
+    stage[e] = reinterpret_cast<const uint4*>(p.pool + (base + s_node[k]) * p.stride)[c];
   }
   __syncthreads();
   for (int e = tid; e < n * kRowChunks; e += blockDim.x) {
@@ -105,6 +108,25 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) compact_accepted_kernel(Plac
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// A programmatic dependent of the stream's previous kernel: the CTAs may
+// become resident while it finishes; each waits for it (griddepcontrol.wait)
+// before reading anything.
+int launch_dependent(void (*kernel)(PlaceParams), dim3 grid, int smem, va_stream_t stream,
+                     const PlaceParams& p) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPlaceWarps * 32, 1u, 1u);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess ? VA_OK : VA_ERR_LAUNCH;
+}
 
 int check_common(const void* pool, int64_t num_slots, int64_t stride, const int64_t* kv_start,
                  const int32_t* prefix_len, const int32_t* capacity, int B, int T,
@@ -147,9 +169,8 @@ VA_API int va_kv_append_contiguous(void* kv_pool, int64_t num_slots, int64_t kv_
   p.B = B;
   p.T = T;
   const int rows = B * T;
-  append_contiguous_kernel<<<(rows + kPlaceWarps - 1) / kPlaceWarps, kPlaceWarps * 32, 0,
-                             reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? VA_OK : VA_ERR_LAUNCH;
+  return launch_dependent(append_contiguous_kernel, dim3(unsigned((rows + kPlaceWarps - 1) / kPlaceWarps)),
+                          0, stream, p);
 }
 
 VA_API int va_kv_compact_accepted(void* kv_pool, int64_t num_slots, int64_t kv_row_stride,
@@ -180,6 +201,5 @@ VA_API int va_kv_compact_accepted(void* kv_pool, int64_t num_slots, int64_t kv_r
   p.status = status;
   p.B = B;
   p.T = T;
-  compact_accepted_kernel<<<B, kPlaceWarps * 32, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? VA_OK : VA_ERR_LAUNCH;
+  return launch_dependent(compact_accepted_kernel, dim3(unsigned(B)), smem, stream, p);
 }
