@@ -26,11 +26,13 @@
  *    by the caller).
  *  - Step-varying data (prefix lengths, slot tables, tree parents) is read on
  *    the device, so one captured graph replays across decode steps.
- *  - Stream order holds as for any launch.  The attention calls' first kernel
- *    is a programmatic dependent of the stream's previous kernel: its CTAs
- *    may become resident while that kernel finishes, but read no input until
- *    it has completed (griddepcontrol.wait).  Their last kernel lets the
- *    stream's next kernel do the same once it has itself passed that point,
+ *  - Stream order holds as for any launch.  The first kernel of the attention
+ *    calls and of the placement calls (va_kv_append_contiguous,
+ *    va_kv_compact_accepted) is a programmatic dependent of the stream's
+ *    previous kernel: its CTAs may become resident while that kernel
+ *    finishes, but read no input until it has completed (griddepcontrol.wait).
+ *    Their last kernel lets the stream's next kernel do the same once it has
+ *    itself passed that point,
  *    so a caller's next kernel launched as a programmatic dependent must wait
  *    (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads the
  *    call's outputs; a plainly launched one is ordered as usual.
