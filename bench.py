@@ -1087,11 +1087,11 @@ def main():
                        nsplit=step.nsplit, path=["auto", "fma", "tc"][args.path],
                        l2=f"inputs larger than L2: {step.nrot} rotating slot tables "
                           f"({step.nrot * kv_step / 1e6:.0f} MB of rows vs {l2 / 1e6:.0f} MB L2)",
-                       launch=f"CUDA graphs of {STEPS_PER_GRAPH} steps (plus one graph of the "
-                              f"{args.steps % STEPS_PER_GRAPH} remaining steps when --steps is "
-                              f"not a multiple of {STEPS_PER_GRAPH}): exactly --steps steps "
-                              "timed; programmatic dependent launch between the kernels of a "
-                              "step and between steps",
+                       launch=f"CUDA graphs of {STEPS_PER_GRAPH} steps"
+                              + (f" plus one graph of the remaining {args.steps % STEPS_PER_GRAPH}"
+                                 if args.steps % STEPS_PER_GRAPH else "")
+                              + ": exactly --steps steps timed; programmatic dependent launch "
+                              "between the kernels of a step and between steps",
                        parallelism=f"replicas x{world}"),
         "headline": head,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
