@@ -237,6 +237,23 @@ def test_contiguous_matches_oracle_and_paged(va, path):
     assert torch.equal(out_c, out_p) and torch.equal(lse_c, lse_p)
 
 
+@pytest.mark.parametrize("path", list(PATHS.values()), ids=list(PATHS))
+@pytest.mark.parametrize("H", [8, 64])
+def test_contiguous_canary_padded_rows(va, path, H):
+    """Contiguous pools of 640-element rows whose padding columns, and every
+    row outside the requests' ranges, hold bf16 NaN: the TMA boxes (whole
+    tiles) and the copies (ragged tiles) read only the requests' rows and their
+    576 columns.  H=8 runs one-SM products, H=64 two-SM products."""
+    s = synth.Spec("contig_canary", B=2, H=H, T=16, prefix=[2000, 777], num_slots=1 << 13,
+                   layout="contiguous", seed=91 + H, canary=True, row_stride=640)
+    _need(va, path, s.B, s.T, s.H)
+    w = synth.make(s)
+    d = _gpu.to_device(w)
+    out, lse = _gpu.run(va, d, w, path=path, layout="contiguous")
+    ref_o, ref_l = _gpu.reference(w)
+    _gpu.compare(out, lse, ref_o, ref_l)
+
+
 @pytest.mark.parametrize("nsplit", [0, 3, 11])
 def test_contiguous_full_h_row_blocks(va, nsplit):
     """Contiguous pools at H=64, T=16 (eight 128-row blocks per request): the
