@@ -199,7 +199,9 @@ def _append_case(va, spec, path, stride=576):
     synth.Spec("app_tp8", B=1, H=8, T=16, prefix=[4096], num_slots=1 << 15, seed=71),
     synth.Spec("app_ragged", B=3, H=8, T=9, prefix=[0, 300, 77], num_slots=8192, seed=72),
     synth.Spec("app_long", B=1, H=8, T=16, prefix=[20000], num_slots=1 << 16, seed=73),
-], ids=["tp8", "ragged", "long"])
+    # two-SM products: the draft keys are read by the QK pair and the PV pair
+    synth.Spec("app_h64", B=2, H=64, T=16, prefix=[1500, 333], num_slots=1 << 14, seed=76),
+], ids=["tp8", "ragged", "long", "h64"])
 def test_segmented_append_then_verify(va, spec, path):
     _append_case(va, spec, path)
 
