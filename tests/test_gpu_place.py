@@ -84,6 +84,42 @@ def test_append_and_compact_match_the_oracle(va, stride):
     assert bad == 2 and int(status.item()) == va.STATUS_BAD_DST
 
 
+def test_append_and_compact_64_node_trees(va):
+    """T = 64 (the largest tree): the compaction stages up to 64 rows (72 KB,
+    past the default 48 KB of dynamic shared memory) before writing any; long
+    accepted paths in any order, against the oracle byte for byte."""
+    g = torch.Generator().manual_seed(64)
+    rng = np.random.default_rng(64)
+    B, T, cap = 3, 64, 400
+    pool = synth._bf16_normal((B * cap + 7, 576), g)
+    ks = np.array([7 + b * cap for b in range(B)], dtype=np.int64)
+    pl = np.array([100, 0, cap - T], dtype=np.int32)
+    caps = np.full(B, cap, dtype=np.int32)
+    draft = synth._bf16_normal((B * T, 576), g)
+    d_pool = pool.cuda()
+    d_ks, d_pl, d_cap = (torch.from_numpy(x).cuda() for x in (ks, pl, caps))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    loc = torch.full((B * T,), 7, dtype=torch.int32, device="cuda")
+    va.kv_append_contiguous(d_pool, d_ks, d_pl, d_cap, draft.cuda(), loc, status=status)
+    p1, loc_w, bad = oracle.append_contiguous(synth.as_u16(pool), synth.as_u16(draft), ks, pl,
+                                              caps, T)
+    torch.cuda.synchronize()
+    assert bad == 0 and int(status.item()) == 0
+    np.testing.assert_array_equal(loc.cpu().numpy(), loc_w)
+    np.testing.assert_array_equal(_u16(d_pool), p1)
+    alen = np.array([64, 37, 5], dtype=np.int32)
+    nodes = np.full((B, T), -1, dtype=np.int32)
+    for b in range(B):
+        nodes[b, :alen[b]] = rng.permutation(T)[:alen[b]]
+    va.kv_compact_accepted(d_pool, d_ks, d_pl, d_cap, torch.from_numpy(alen).cuda(),
+                           torch.from_numpy(nodes).cuda(), status=status)
+    torch.cuda.synchronize()
+    p2, pl_w, bad = oracle.compact_accepted(p1, ks, pl, caps, alen, nodes, T)
+    assert bad == 0 and int(status.item()) == 0
+    np.testing.assert_array_equal(_u16(d_pool), p2)
+    np.testing.assert_array_equal(d_pl.cpu().numpy(), pl_w)
+
+
 def _logits_for(rng, par, tok, V, follow=0.8):
     """Target logits whose greedy token at the prefix and at each node is, with
     probability `follow`, the token of one of that position's children."""
